@@ -1,0 +1,521 @@
+"""Benchmark of the Token Recycling per-step hot path on one GB300 (or N, weak scaling).
+
+A step is one pass of the whole hot path over one batch: tree-attention
+verification (tr_verify_attn), then tr_step (top-K or fused LM head + top-K,
+greedy acceptance, matrix update, KV commit, next tree retrieval).  The
+synthetic target that produces each step's logits depends on that step's
+tree, so the timed run replays a recording: the loop first runs with the
+device-side target, storing every step's logits (or hidden states) and
+attention operands in HBM; the state is then restored and the same steps run
+again with only the hot-path kernels inside the timed region.  The replay must
+end in the recorded state, which is checked.  Inputs of every step are larger
+than L2 (fresh logits and the KV cache), so no flush is needed between steps.
+
+Default workload: 16 sequences with their own matrices (V=32000, K=8, int64),
+80-node tree, prefixes uniform in 1k..4k, 32 heads x 128, fp32 logits.
+
+--impl reference times the CPU oracle (a deliberately plain program) on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# dram bytes per launch of the dominant kernel from an ncu capture, valid only
+# while the kernel source is unchanged (sha256 of its .cu file)
+TRAFFIC = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAK_FALLBACK, "fallback"
+
+
+def src_sha(name):
+    p = os.path.join(ROOT, "free_speculative_decoding_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def attn_bytes(w, N, L):
+    """Algorithmic HBM bytes of one tr_verify_attn launch with cache lengths L[b]:
+    cached K and V read once, tree Q/K/V read once, fp32 O written once."""
+    kv = 2 * 2 * w.Hkv * w.d * int(np.sum(L))
+    tree = w.B * N * w.d * 2 * (w.Hq + 2 * w.Hkv)
+    out = w.B * N * w.Hq * w.d * 4
+    return kv + tree + out
+
+
+def launches_per_step(w):
+    """libtr kernels launched by one timed step: verify attention (1), then
+    tr_step = top-K (1) or fused LM head (tile + merge, 2), and the fused
+    accept/update/commit/retrieve kernel (1)."""
+    return (1 if w.attention else 0) + (2 if w.logits == "lmhead" else 1) + 1
+
+
+def topk_bytes(w, N):
+    esz = 2 if w.logits == "bf16" else 4
+    return w.B * N * w.V * esz
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    import free_speculative_decoding_gb300 as tr
+    from free_speculative_decoding_gb300.engine import TRState
+    from synth import device as sd
+
+    w = synth.WORKLOADS[args.workload]
+    if world > 1:
+        w = w.scaled(seed=w.seed + 1000 * rank)   # each rank decodes its own sequences
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    tree = tr.Tree(w.child_counts, w.K)
+    N = tree.N
+    mdt = torch.int64 if w.m_dtype == "int64" else torch.int32
+    ldt = torch.bfloat16 if w.logits == "bf16" else torch.float32
+    lm = w.logits == "lmhead"
+    W, K = args.warmup, args.steps
+    cap = int(w.prefix[1]) + (W + K) * (tree.max_depth + 1)
+    st = TRState(tree, w.B, w.V, m_dtype=mdt, Hq=w.Hq if w.attention else 0, Hkv=w.Hkv, d=w.d, cap=cap,
+                 logits_dtype=ldt, D=w.D if lm else 0, device=dev)
+    tgt = sd.DeviceTarget(w, tree, dev)
+    sd.warm_matrices(w, st)
+    if w.attention:
+        sd.fill_cache(w, st)
+    st.start(synth.initial_roots(w), w.prefix_lengths(), M_src=st.M.clone())
+    stream = torch.cuda.current_stream()
+
+    # per-step input sizes
+    if lm:
+        step_in = w.B * N * w.D * 2
+    else:
+        step_in = w.B * N * w.V * (2 if w.logits == "bf16" else 4)
+    qkv_b = w.B * N * w.d * 2 * (w.Hq + 2 * w.Hkv) if w.attention else 0
+    budget = args.store_gb * 2 ** 30
+    seg = max(1, min(K, int(budget // max(1, step_in + qkv_b))))
+
+    def make_bufs(n):
+        bufs = {}
+        if lm:
+            bufs["H"] = torch.empty(n, w.B * N, w.D, dtype=torch.bfloat16, device=dev)
+        else:
+            bufs["logits"] = torch.empty(n, w.B * N, w.V, dtype=ldt, device=dev)
+        if w.attention:
+            bufs["q"] = torch.empty(n, w.B, N, w.Hq, w.d, dtype=torch.bfloat16, device=dev)
+            bufs["kt"] = torch.empty(n, w.B, N, w.Hkv, w.d, dtype=torch.bfloat16, device=dev)
+            bufs["vt"] = torch.empty(n, w.B, N, w.Hkv, w.d, dtype=torch.bfloat16, device=dev)
+        return bufs
+
+    bufs = make_bufs(seg)
+    gstep = [0]
+
+    def gen_step(i):
+        """Generate step inputs into slot i for the current tree (the target stand-in)."""
+        s = gstep[0]
+        if w.attention:
+            sd.step_qkv(w, s, N, dev, out=(bufs["q"][i], bufs["kt"][i], bufs["vt"][i]))
+        if lm:
+            tgt.hidden_for(st, bufs["H"][i])
+        else:
+            tgt.logits_for(st, bufs["logits"][i])
+        gstep[0] += 1
+
+    def hot_step(i, ev=None):
+        kt = vt = None
+        if ev is not None:
+            ev[0].record(stream)
+        if w.attention:
+            kt, vt = bufs["kt"][i], bufs["vt"][i]
+            st.verify(bufs["q"][i], kt, vt)
+        if ev is not None:
+            ev[1].record(stream)
+        if lm:
+            st.finish(H=bufs["H"][i], Wt=tgt.Wt, Kt=kt, Vt=vt)
+        else:
+            st.finish(logits=bufs["logits"][i], Kt=kt, Vt=vt)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def snapshot():
+        snap = {"M": st.M.clone(), "root": st.root.clone(), "L": st.L.clone(), "tok": st.tree_tok.clone()}
+        return snap
+
+    def restore(snap):
+        st.M.copy_(snap["M"])
+        st.root.copy_(snap["root"])
+        st.L.copy_(snap["L"])
+        st.tree_tok.copy_(snap["tok"])
+
+    # warm-up: W full steps (target + hot path), untimed
+    for _ in range(W):
+        gen_step(0)
+        hot_step(0)
+    torch.cuda.synchronize()
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+    total_ms = 0.0
+    attn_ms, step_ms = [], []
+    attn_bytes_list = []
+    done = 0
+    replay_ok = True
+    committed = 0
+    clocks = ClockSampler(dev.index)
+    clocks_started = False
+    while done < K:
+        n = min(seg, K - done)
+        snap = snapshot()
+        L_hist = []
+        # record: the target writes each step's inputs for the tree of that step
+        for i in range(n):
+            L_hist.append(st.L.clone())
+            gen_step(i)
+            hot_step(i)
+        ref_state = (st.M.clone(), st.L.clone(), st.root.clone())
+        restore(snap)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if not clocks_started:
+            clocks.start()
+            clocks_started = True
+            time.sleep(0.3)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(n):
+            hot_step(i, evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        total_ms += start.elapsed_time(stop)
+        for i in range(n):
+            if w.attention:
+                attn_ms.append(evs[i][0].elapsed_time(evs[i][1]))
+                attn_bytes_list.append(attn_bytes(w, N, L_hist[i].cpu().numpy()))
+            step_ms.append(evs[i][1].elapsed_time(evs[i][2]))
+        replay_ok &= bool(torch.equal(st.M, ref_state[0]) and torch.equal(st.L, ref_state[1])
+                          and torch.equal(st.root, ref_state[2]))
+        committed += int((st.L - snap["L"]).sum().item())
+        done += n
+    clk = clocks.stop()
+    status = st.status()
+
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    res = {"total_ms": total_ms, "attn_ms": attn_ms, "attn_bytes": attn_bytes_list, "replay_ok": replay_ok,
+           "status": status, "clocks": clk, "committed": committed, "N": N, "w": w, "seg": seg,
+           "step_ms": step_ms}
+
+    # end to end through the public calls with host buffers (rank 0 and every rank alike)
+    if args.e2e_steps > 0:
+        res["e2e"] = run_e2e(args, w, st, tgt, bufs, gen_step, hot_step, snapshot, restore, dev, N, lm)
+    return res
+
+
+def run_e2e(args, w, st, tgt, bufs, gen_step, hot_step, snapshot, restore, dev, N, lm):
+    """Same steps with every step's inputs copied from pinned host memory and the
+    committed tokens read back, all inside the timed region."""
+    import torch
+
+    E = min(args.e2e_steps, bufs["H" if lm else "logits"].shape[0])
+    snap = snapshot()
+    for i in range(E):
+        gen_step(i)
+        hot_step(i)
+    restore(snap)
+    torch.cuda.synchronize()
+    host = {k: torch.empty(v[:E].shape, dtype=v.dtype, pin_memory=True) for k, v in bufs.items()}
+    for k in host:
+        host[k].copy_(bufs[k][:E])
+    out_acc = torch.empty(E, w.B, dtype=torch.int32, pin_memory=True)
+    out_com = torch.empty(E, w.B, st.committed.shape[1], dtype=torch.int32, pin_memory=True)
+    h2d = sum(host[k][0].numel() * host[k][0].element_size() for k in host)
+    d2h = out_acc[0].numel() * 4 + out_com[0].numel() * 4
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(E):
+        for k in host:
+            bufs[k][0].copy_(host[k][i], non_blocking=True)
+        hot_step(0)
+        out_acc[i].copy_(st.acc_len, non_blocking=True)
+        out_com[i].copy_(st.committed, non_blocking=True)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = start.elapsed_time(stop)
+    restore(snap)
+    return {"steps": E, "ms": ms, "wall_s": wall, "h2d": int(h2d), "d2h": int(d2h)}
+
+
+# ----------------------------------------------------------------------------
+# oracle arm (CPU)
+# ----------------------------------------------------------------------------
+
+def oracle_sequence_step(w, b, state, plan, step):
+    """One Token Recycling step of sequence b on the CPU oracle; returns seconds
+    spent in the method (the synthetic target's logits are made before timing)."""
+    import oracle
+    depth = np.asarray(plan.depth)
+    tok = oracle.retrieve(state.M, state.root, plan)
+    if w.logits == "lmhead":
+        H = synth.bf16_to_f32(synth.lm_hidden_rows(w.seed, b, state.L + depth, tok, w.D))
+        Wt = _lm_weight_cache(w)
+        t0 = time.perf_counter()
+        tok = oracle.retrieve(state.M, state.root, plan)
+        rows = oracle.lmhead_logits(H, Wt)
+    else:
+        rows = synth.logits_f32(w.seed, b, state.L + depth, tok, w.V, w.logits)
+        qkv = None
+        if w.attention:
+            q, kt, vt = synth.step_qkv(w, step, [b])
+            qkv = (synth.bf16_to_f32(q[0]), synth.bf16_to_f32(kt[0]), synth.bf16_to_f32(vt[0]))
+        t0 = time.perf_counter()
+        tok = oracle.retrieve(state.M, state.root, plan)
+        if qkv is not None:
+            oracle.tree_attention(qkv[0], state.kc, state.vc, state.L, qkv[1], qkv[2], plan, w.d ** -0.5)
+    ids, _ = oracle.topk_rows(rows, w.K)
+    acc, path, committed, bonus = oracle.accept(plan, tok, ids[:, 0])
+    oracle.update(state.M, tok, ids, plan)
+    if w.attention and state.kc is not None:
+        state.L = oracle.kv_commit(state.kc, state.vc, qkv[1], qkv[2], state.L, path)
+    else:
+        state.L += len(path)
+    state.root = bonus
+    return time.perf_counter() - t0
+
+
+_LMW = {}
+
+
+def _lm_weight_cache(w):
+    if w.name not in _LMW:
+        _LMW[w.name] = synth.bf16_to_f32(synth.lm_weight_rows(w.seed, w.V, w.D)).astype(np.float64)
+    return _LMW[w.name]
+
+
+def oracle_rate(w, budget_s, max_seq_steps=None):
+    """Oracle steps/s of the full batch, extrapolated from a bounded sample of
+    sequence-steps of one sequence (each sequence is independent and alike)."""
+    import oracle
+    plan = oracle.TreePlan(w.child_counts, w.K)
+    b = 0
+    L0 = int(w.prefix_lengths()[b])
+    st = oracle.TRState(M=synth.warm_matrix(w.seed, b, w.V, w.K), root=int(synth.initial_roots(w)[b]), L=L0)
+    if w.attention:
+        cap = L0 + 64 * (plan.max_depth + 1)
+        st.kc = np.zeros((w.Hkv, cap, w.d), np.float32)
+        st.vc = np.zeros_like(st.kc)
+        hh, pp = np.meshgrid(np.arange(w.Hkv), np.arange(L0), indexing="ij")
+        st.kc[:, :L0] = synth.bf16_to_f32(synth.kc_rows(w.seed, b, hh, pp, w.d)).reshape(w.Hkv, L0, w.d)
+        st.vc[:, :L0] = synth.bf16_to_f32(synth.vc_rows(w.seed, b, hh, pp, w.d)).reshape(w.Hkv, L0, w.d)
+    spent, n = 0.0, 0
+    while spent < budget_s and (max_seq_steps is None or n < max_seq_steps) and n < 64:
+        spent += oracle_sequence_step(w, b, st, plan, n)
+        n += 1
+    per_seq_step = spent / n
+    return 1.0 / (per_seq_step * w.B), n, spent
+
+
+def cpu_cores():
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", default="tr", choices=["tr", "reference"])
+    ap.add_argument("--workload", default="batched", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--store-gb", type=float, default=40.0, help="HBM for recorded step inputs")
+    ap.add_argument("--e2e-steps", type=int, default=16)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    w = synth.WORKLOADS[args.workload]
+    metric = "TR steps/s"
+    unit = "steps/s (%d sequences x %d-node tree per step)" % (w.B, w.N)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+        import oracle  # noqa: F401
+        oracle_rate(w, budget_s=1e9, max_seq_steps=max(1, args.warmup))   # warm-up steps
+        rate, n, spent = oracle_rate(w, budget_s=per_step * args.steps, max_seq_steps=args.steps)
+        line = {"impl": "reference", "metric": metric, "value": rate, "unit": unit, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / rate, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention / exact compare", "data": "synthetic",
+                "config": {"workload": args.workload},
+                "cpu_baseline": {"value": rate, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
+                                 "sample": "%d sequence-steps of sequence 0 (%.1f s), scaled to %d sequences"
+                                           % (n, spent, w.B)},
+                "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
+    res = run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    K = args.steps
+    wl = res["w"]
+    N = res["N"]
+    ms_per_step = res["total_ms"] / K
+    value = world * 1e3 / ms_per_step       # whole-job steps/s (each rank its own batch)
+    peaks, peak_kind = load_peaks()
+    roofline = None
+    if wl.attention and res["attn_ms"]:
+        a_ms = float(np.mean(res["attn_ms"]))
+        a_bytes = float(np.mean(res["attn_bytes"]))
+        ach = a_bytes / (a_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        tr_ = TRAFFIC.get("attn")
+        traffic = tr_["bytes"] if tr_ and tr_["sha"] == src_sha("tr_attn.cu") else None
+        roofline = {"kernel": "tr_verify_attn", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                    "frac": ach / peak, "traffic": traffic, "peak_source": peak_kind,
+                    "algorithmic_bytes_per_launch": a_bytes, "ms_per_launch": a_ms}
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 attention (fp32 accumulate), %s logits, int64/int32 state" % wl.logits,
+        "data": "synthetic (seeded splitmix64 target; see DESIGN.md)",
+        "config": {"workload": args.workload, "B": wl.B, "V": wl.V, "K": wl.K, "tree_nodes": N,
+                   "prefix": list(wl.prefix), "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "parallelism": "replicas (dp%d, no collective)" % world,
+                   "l2": "per-step inputs larger than L2 (fresh logits + KV cache)",
+                   "timed": "record-then-replay: hot-path kernels only"},
+        "tree_tokens_per_s": value * wl.B * N,
+        "committed_tokens_per_s": world * res["committed"] / (res["total_ms"] * 1e-3),
+        "mat": res["committed"] / (K * wl.B),
+        "replay_matches_record": res["replay_ok"], "device_status": res["status"],
+        "gpu_launches": K * launches_per_step(wl),
+        "clocks": res["clocks"],
+    }
+    if res["step_ms"]:
+        line["tr_step_ms"] = float(np.mean(res["step_ms"]))
+        line["topk_bytes_per_launch"] = topk_bytes(wl, N)
+    if roofline:
+        line["roofline"] = roofline
+    if "e2e" in res:
+        e = res["e2e"]
+        line["e2e"] = {"value": world * e["steps"] / (e["ms"] * 1e-3), "unit": unit, "h2d_bytes_per_step": e["h2d"],
+                       "d2h_bytes_per_step": e["d2h"], "steps": e["steps"]}
+    # the oracle on a bounded sample of the same workload, on this host's cores
+    rate, n, spent = oracle_rate(wl, budget_s=args.cpu_budget)
+    line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
+                            "sample": "%d sequence-steps of sequence 0 (%.1f s of oracle time), scaled to %d "
+                                      "sequences; BLAS calls may use all cores" % (n, spent, wl.B)}
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

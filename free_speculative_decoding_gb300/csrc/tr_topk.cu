@@ -1,0 +1,209 @@
+// Per-row top-K over vocabulary logits (fp32 or bf16), ties to the lower ID.
+//
+// The kernel streams each row once from HBM with 16-byte loads.  A row is cut
+// into `splits` chunks of about 8K elements so that the grid holds several
+// waves of short CTAs on 152 SMs whatever the row count.  Each thread keeps a
+// sorted register list of 64-bit keys (order-preserving value code in the
+// high word, complemented ID in the low word, so larger key = better and equal
+// values prefer the lower ID); a one-compare float threshold rejects almost
+// every element.  Lists merge by warp shuffles, then across warps, then across
+// the row's chunks in the last CTA to finish (an arrival counter in the
+// workspace, no spin-wait).
+#include "tr_internal.cuh"
+#include "tr_lists.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+constexpr long long kChunk = 8192;  // target elements per CTA
+constexpr int kMaxSplits = 32;
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+  static constexpr int kVec = 4;
+  template <int KMAX>
+  __device__ __forceinline__ static void push_vec(TopList<KMAX> &L, const uint4 &q, uint32_t id) {
+    L.push(__uint_as_float(q.x), id);
+    L.push(__uint_as_float(q.y), id + 1);
+    L.push(__uint_as_float(q.z), id + 2);
+    L.push(__uint_as_float(q.w), id + 3);
+  }
+  __device__ __forceinline__ static float load1(const float *p) { return __ldcs(p); }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  template <int KMAX>
+  __device__ __forceinline__ static void push_vec(TopList<KMAX> &L, const uint4 &q, uint32_t id) {
+    L.push(__uint_as_float(q.x << 16), id);
+    L.push(__uint_as_float(q.x & 0xFFFF0000u), id + 1);
+    L.push(__uint_as_float(q.y << 16), id + 2);
+    L.push(__uint_as_float(q.y & 0xFFFF0000u), id + 3);
+    L.push(__uint_as_float(q.z << 16), id + 4);
+    L.push(__uint_as_float(q.z & 0xFFFF0000u), id + 5);
+    L.push(__uint_as_float(q.w << 16), id + 6);
+    L.push(__uint_as_float(q.w & 0xFFFF0000u), id + 7);
+  }
+  __device__ __forceinline__ static float load1(const __nv_bfloat16 *p) {
+    const unsigned short u = __ldcs((const unsigned short *)p);
+    return __uint_as_float((uint32_t)u << 16);
+  }
+};
+
+template <typename T, int KMAX, bool VEC>
+__global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long long V, long long ld, int K,
+                                                        long long chunk, int32_t *ids, float *vals,
+                                                        unsigned long long *part, unsigned *counters) {
+  __shared__ unsigned long long warp_keys[kThreads / 32][KMAX];
+  __shared__ int is_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int split = blockIdx.x, splits = gridDim.x;
+  const long long row = blockIdx.y;
+  const T *x = logits + row * ld;
+  const long long lo = split * chunk;
+  const long long hi = min(V, lo + chunk);
+
+  TopList<KMAX> L;
+  L.init();
+  long long done = lo;
+  if (VEC) {
+    constexpr int kV = Elem<T>::kVec;
+    const uint4 *xv = reinterpret_cast<const uint4 *>(x + lo);
+    const int nvec = (int)((hi - lo) / kV);
+    for (int i0 = tid; i0 < nvec; i0 += kThreads * kUnroll) {
+      uint4 buf[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = i0 + u * kThreads;
+        if (i < nvec) buf[u] = __ldcs(xv + i);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int i = i0 + u * kThreads;
+        if (i < nvec) Elem<T>::template push_vec<KMAX>(L, buf[u], (uint32_t)(lo + (long long)i * kV));
+      }
+    }
+    done = lo + (long long)nvec * kV;
+  }
+  for (long long i = done + tid; i < hi; i += kThreads) L.push(Elem<T>::load1(x + i), (uint32_t)i);
+
+  // block merge
+  unsigned long long mine = warp_merge<KMAX>(L, lane);
+  if (lane < KMAX) warp_keys[warp][lane] = mine;
+  __syncthreads();
+  if (warp != 0) return;
+  L.init();
+  if (lane < kThreads / 32) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) L.k[j] = warp_keys[lane][j];
+  }
+  mine = warp_merge<KMAX>(L, lane);
+
+  if (splits > 1) {
+    // publish this chunk's list; the row's last CTA to arrive merges them all
+    if (lane < KMAX) part[(row * splits + split) * KMAX + lane] = mine;
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) is_last = atomicAdd(&counters[row], 1u) == (unsigned)(splits - 1);
+    __syncwarp();
+    if (!is_last) return;
+    __threadfence();
+    L.init();
+    for (int sp = lane; sp < splits; sp += 32) {
+      const unsigned long long *src = part + (row * splits + sp) * KMAX;
+      for (int j = 0; j < KMAX; ++j) {
+        const unsigned long long key = __ldcg(src + j);
+        if (key == 0ull) break;
+        list_insert<KMAX>(L.k, key);
+      }
+    }
+    mine = warp_merge<KMAX>(L, lane);
+    if (lane == 0) counters[row] = 0u;
+  }
+  if (lane < K) {
+    ids[row * K + lane] = mine ? (int32_t)tr_key_id(mine) : -1;
+    if (vals) vals[row * K + lane] = mine ? tr_key_val(mine) : -INFINITY;
+  }
+}
+
+template <typename T, int KMAX>
+void launch(const void *logits, long long rows, long long V, long long ld, int K, int splits, long long chunk,
+            bool vec, int32_t *ids, float *vals, void *ws, size_t part_bytes, cudaStream_t s) {
+  unsigned long long *part = (unsigned long long *)ws;
+  unsigned *counters = (unsigned *)((char *)ws + part_bytes);
+  dim3 grid(splits, (unsigned)rows);
+  if (vec)
+    topk_kernel<T, KMAX, true><<<grid, kThreads, 0, s>>>((const T *)logits, V, ld, K, chunk, ids, vals, part, counters);
+  else
+    topk_kernel<T, KMAX, false><<<grid, kThreads, 0, s>>>((const T *)logits, V, ld, K, chunk, ids, vals, part,
+                                                          counters);
+}
+
+long long plan_chunk(long long V, int splits) {
+  // chunks are multiples of 8 elements so every chunk of an aligned row is 16-byte aligned
+  long long c = (V + splits - 1) / splits;
+  return (c + 7) / 8 * 8;
+}
+
+size_t part_bytes_for(long long rows, int splits, int K) {
+  return splits > 1 ? tr_align_up((size_t)rows * splits * tr_kmax(K) * 8, 256) : 0;
+}
+
+}  // namespace
+
+int tr_topk_plan_splits(int64_t rows, int64_t V) {
+  (void)rows;
+  long long s = (V + kChunk - 1) / kChunk;
+  if (s < 1) s = 1;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return (int)s;
+}
+
+extern "C" size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K) {
+  if (rows <= 0 || V <= 0 || K < 1 || K > TR_MAX_K) return 0;
+  const int splits = tr_topk_plan_splits(rows, V);
+  if (splits == 1) return 0;
+  return part_bytes_for(rows, splits, K) + tr_align_up((size_t)rows * 4, 256);
+}
+
+int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K, int32_t *ids,
+                   float *vals, void *ws, size_t ws_bytes, cudaStream_t s) {
+  const int splits = tr_topk_plan_splits(rows, V);
+  const long long chunk = splits > 1 ? plan_chunk(V, splits) : V;
+  const size_t esz = ftype == TR_F32 ? 4 : 2;
+  const bool vec = ((uintptr_t)logits % 16 == 0) && ((ld * (int64_t)esz) % 16 == 0);
+  const size_t pb = part_bytes_for(rows, splits, K);
+  const int km = tr_kmax(K);
+#define TR_TOPK_CASE(T, KM) launch<T, KM>(logits, rows, V, ld, K, splits, chunk, vec, ids, vals, ws, pb, s)
+  if (ftype == TR_F32) {
+    if (km == 8) TR_TOPK_CASE(float, 8);
+    else if (km == 16) TR_TOPK_CASE(float, 16);
+    else TR_TOPK_CASE(float, 32);
+  } else {
+    if (km == 8) TR_TOPK_CASE(__nv_bfloat16, 8);
+    else if (km == 16) TR_TOPK_CASE(__nv_bfloat16, 16);
+    else TR_TOPK_CASE(__nv_bfloat16, 32);
+  }
+#undef TR_TOPK_CASE
+  TR_LAUNCH_CHECK();
+  (void)ws_bytes;
+  return TR_OK;
+}
+
+extern "C" int tr_topk(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K, int32_t *ids,
+                       float *vals, void *ws, size_t ws_bytes, tr_stream_t stream) {
+  if (rows < 0 || V < 1 || K < 1 || K > TR_MAX_K || K > V || ld < V) return TR_E_INVAL;
+  if (ftype != TR_F32 && ftype != TR_BF16) return TR_E_INVAL;
+  if (V > INT32_MAX) return TR_E_UNSUPPORTED;
+  if (rows == 0) return TR_OK;
+  if (!logits || !ids) return TR_E_INVAL;
+  const size_t need = tr_topk_workspace_bytes(rows, V, K);
+  if (need && (!ws || ws_bytes < need)) return TR_E_INVAL;
+  if (rows > 65535) return TR_E_UNSUPPORTED;  // grid.y limit
+  int rc = tr_check_device();
+  if (rc != TR_OK) return rc;
+  return tr_topk_launch(logits, ftype, rows, V, ld, K, ids, vals, ws, ws_bytes, (cudaStream_t)stream);
+}

@@ -299,14 +299,16 @@ def vc_rows(seed, b, h, pos, d):
     return noise_rows_bf16(hkey(seed, TAG_VC, b, h, pos), d)
 
 
-def step_qkv(w: Workload, step):
-    """Q [B,N,Hq,d], Kt/Vt [B,N,Hkv,d] of one step as bf16 bit patterns."""
-    B, N, Hq, Hkv, d = w.B, w.N, w.Hq, w.Hkv, w.d
-    b, n, h = np.meshgrid(np.arange(B), np.arange(N), np.arange(Hq), indexing="ij")
-    q = q_rows(w.seed, step, b, n, h, d).reshape(B, N, Hq, d)
-    b, n, h = np.meshgrid(np.arange(B), np.arange(N), np.arange(Hkv), indexing="ij")
-    kt = kt_rows(w.seed, step, b, n, h, d).reshape(B, N, Hkv, d)
-    vt = vt_rows(w.seed, step, b, n, h, d).reshape(B, N, Hkv, d)
+def step_qkv(w: Workload, step, seqs=None):
+    """Q [S,N,Hq,d], Kt/Vt [S,N,Hkv,d] of one step as bf16 bit patterns, for the
+    sequences ``seqs`` (all B by default)."""
+    seqs = np.arange(w.B) if seqs is None else np.asarray(seqs)
+    S, N, Hq, Hkv, d = len(seqs), w.N, w.Hq, w.Hkv, w.d
+    b, n, h = np.meshgrid(seqs, np.arange(N), np.arange(Hq), indexing="ij")
+    q = q_rows(w.seed, step, b, n, h, d).reshape(S, N, Hq, d)
+    b, n, h = np.meshgrid(seqs, np.arange(N), np.arange(Hkv), indexing="ij")
+    kt = kt_rows(w.seed, step, b, n, h, d).reshape(S, N, Hkv, d)
+    vt = vt_rows(w.seed, step, b, n, h, d).reshape(S, N, Hkv, d)
     return q, kt, vt
 
 
@@ -391,22 +393,31 @@ def lm_weight_rows(seed, V, D, v_lo=0, v_hi=None):
     target toward a low-rank Markov table.
     """
     v_hi = V if v_hi is None else v_hi
-    v = np.arange(v_lo, v_hi)
+    out = np.empty((v_hi - v_lo, D), dtype=np.uint16)
     i = np.arange(D)
-    noise = irwin_hall12(hkey(seed, TAG_W, v)[:, None], i[None, :]) * np.float32(LM_W_STD)
-    w = np.rint(noise.astype(np.float32) * np.float32(LM_W_GRID)) / np.float32(LM_W_GRID)
     succ = lm_successor(seed, V)
     pat = lm_pattern(seed, D)
-    for c in range(LM_CLASSES):
-        hit = v == succ[c]
-        if hit.any():
-            w[hit] += np.float32(LM_W_BIAS) * pat[c]
-    return bf16_bits(w.astype(np.float32))
+    for lo in range(v_lo, v_hi, _ROW_CHUNK):
+        v = np.arange(lo, min(v_hi, lo + _ROW_CHUNK))
+        noise = irwin_hall12(hkey(seed, TAG_W, v)[:, None], i[None, :]) * np.float32(LM_W_STD)
+        w = np.rint(noise.astype(np.float32) * np.float32(LM_W_GRID)) / np.float32(LM_W_GRID)
+        for c in range(LM_CLASSES):
+            hit = v == succ[c]
+            if hit.any():
+                w[hit] += np.float32(LM_W_BIAS) * pat[c]
+        out[lo - v_lo:lo - v_lo + len(v)] = bf16_bits(w.astype(np.float32))
+    return out
+
+
+_ROW_CHUNK = 1024
 
 
 def lm_realistic(seed, rows, V, D):
     """Off-grid bf16 operands (H ~ N(0,1), Wt ~ N(0, 0.02^2)) for the tolerance test."""
     h = noise_rows_bf16(hkey(seed, TAG_H, 7, np.arange(rows)), D)
-    wn = irwin_hall12(hkey(seed, TAG_W, 7, np.arange(V))[:, None], np.arange(D)[None, :])
-    wt = bf16_bits((wn * np.float32(LM_W_STD)).astype(np.float32))
+    wt = np.empty((V, D), dtype=np.uint16)
+    for lo in range(0, V, _ROW_CHUNK):
+        v = np.arange(lo, min(V, lo + _ROW_CHUNK))
+        wn = irwin_hall12(hkey(seed, TAG_W, 7, v)[:, None], np.arange(D)[None, :])
+        wt[lo:lo + len(v)] = bf16_bits((wn * np.float32(LM_W_STD)).astype(np.float32))
     return h, wt

@@ -1,0 +1,92 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+rejects bad arguments on the host, and builds the same tree plans as the oracle."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from free_speculative_decoding_gb300 import build as b
+    b.build()
+    import free_speculative_decoding_gb300 as tr
+    return tr.lib()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:int|size_t|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import free_speculative_decoding_gb300 as tr
+    names = _declared()
+    assert {"tr_retrieve", "tr_verify_attn", "tr_topk", "tr_lmhead_topk", "tr_accept", "tr_update",
+            "tr_step", "tr_init_matrix", "tr_get_status"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert names == set(tr.ABI_SYMBOLS)
+
+
+def test_tree_plan_matches_oracle(lib):
+    import free_speculative_decoding_gb300 as tr
+    for counts in (synth.TREE_T80, synth.TREE_T128, synth.chain_tree(5), (0,), (3, 2, 1, 0, 0, 0, 0)):
+        t = tr.Tree(counts, 8)
+        p = oracle.TreePlan(counts, 8)
+        assert t.N == p.N and t.max_depth == p.max_depth
+        assert t.parent == p.parent and t.rank == p.rank and t.depth == p.depth
+
+
+@pytest.mark.parametrize("counts,K", [((4, 0, 0), 8), ((1, 0, 1), 8), ((9,) + (0,) * 9, 8), ((), 8),
+                                      ((0,) * 129, 8), ((1, 0), 0), ((1, 0), 33)])
+def test_tree_rejects_bad_specs(lib, counts, K):
+    import free_speculative_decoding_gb300 as tr
+    with pytest.raises(tr.TRError) as e:
+        tr.Tree(counts, K)
+    assert e.value.code == tr.TR_E_INVAL
+
+
+def test_host_validation_before_any_launch(lib):
+    import free_speculative_decoding_gb300 as tr
+    p = ctypes.c_void_p(16)   # never dereferenced: validation fails first
+    ws = ctypes.c_void_p(0)
+    assert lib.tr_topk(p, tr.TR_F32, 4, 10, 10, 11, p, None, ws, 0, None) == tr.TR_E_INVAL      # K > V
+    assert lib.tr_topk(p, tr.TR_F32, 4, 10, 8, 3, p, None, ws, 0, None) == tr.TR_E_INVAL       # ld < V
+    assert lib.tr_topk(p, 7, 4, 10, 10, 3, p, None, ws, 0, None) == tr.TR_E_INVAL               # dtype
+    assert lib.tr_topk(None, tr.TR_F32, 0, 10, 10, 3, None, None, ws, 0, None) == tr.TR_OK       # empty
+    assert lib.tr_lmhead_topk(p, p, 4, 100, 10, 3, p, None, ws, 0, None) == tr.TR_E_UNSUPPORTED  # D % 64
+    assert lib.tr_init_matrix(None, tr.TR_I64, 1, 10, 3, 0, None, 0, None) == tr.TR_E_INVAL
+    assert lib.tr_init_matrix(p, tr.TR_I64, 1, 10, 3, tr.TR_INIT_INHERIT, None, 0, None) == tr.TR_E_INVAL
+    t = tr.Tree(synth.TREE_T80, 8)
+    assert lib.tr_retrieve(p, tr.TR_I64, 1, 100, 4, t.handle, p, p, None) == tr.TR_E_INVAL       # K mismatch
+    assert lib.tr_verify_attn(p, p, p, p, p, p, 64, 1, 6, 4, 128, 0.1, t.handle, p, p, 1 << 30,
+                              None) == tr.TR_E_INVAL                                               # Hq % Hkv
+    assert lib.tr_verify_attn(p, p, p, p, p, p, 64, 1, 4, 4, 64, 0.1, t.handle, p, p, 1 << 30,
+                              None) == tr.TR_E_UNSUPPORTED                                         # d != 128
+    assert lib.tr_update(p, tr.TR_I64, 1, 100, 8, t.handle, p, p, tr.TR_UPD_ACCEPTED, None, None,
+                         None) == tr.TR_E_INVAL
+    assert lib.tr_get_status(None, None) == tr.TR_E_INVAL
+    assert lib.tr_status_string(tr.TR_E_CUDA).startswith(b"TR_E_CUDA")
+
+
+def test_workspace_sizes(lib):
+    import free_speculative_decoding_gb300 as tr
+    # rows that fit one chunk need no workspace; longer rows need list space and counters
+    assert lib.tr_topk_workspace_bytes(10, 4000, 8) == 0
+    assert lib.tr_topk_workspace_bytes(1280, 32000, 8) >= 1280 * 4 * 8 * 8 + 1280 * 4
+    t = tr.Tree(synth.TREE_T80, 8)
+    assert lib.tr_verify_attn_workspace_bytes(16, 32, 32, 128, 5888, t.handle) > 0
+    assert lib.tr_kv_commit_workspace_bytes(16) >= 64

@@ -1,0 +1,159 @@
+"""Multi-step parity of the CUDA Token Recycling loop against the oracle (GB300 only).
+
+The GPU loop runs exactly the calls the benchmark times (tr_verify_attn, then
+tr_step: top-K or fused LM head + top-K, acceptance, update, KV commit, next
+retrieval); the synthetic target is generated on the device.  The oracle
+replays the same seeded loop on the CPU.  Integer state must be bit-exact at
+every step (tree tokens, top-K IDs, accepted lengths, paths, committed
+tokens, every matrix row); attention within 2e-3 per (node, head) row.
+
+Full-size runs are checked on samples the oracle can afford and on the
+losslessness invariant (the committed stream equals plain greedy decoding
+under the target), which holds at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import compare_step, oracle_qkv, oracle_states, rows_rel_err, run_gpu_loop, target_fn, ATTN_TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from free_speculative_decoding_gb300 import build as b
+    b.build()
+
+
+def _check_loop(w, steps, seqs=None, attn=True, M_every=1):
+    plan = oracle.TreePlan(w.child_counts, w.K)
+    recs, st, status = run_gpu_loop(w, steps, keep_M_every=M_every)
+    assert status == 0
+    seqs = list(range(w.B)) if seqs is None else list(seqs)
+    states = oracle_states(w, seqs, with_cache=attn and w.attention)
+    target = target_fn(w)
+
+    def on_step(s, i, rec):
+        b = seqs[i]
+        compare_step(w, plan, s, i, b, rec, recs[s], attn=attn)
+        if "M" in recs[s]:
+            assert np.array_equal(recs[s]["M"][b], states[i].M), "M after step %d seq %d" % (s, b)
+
+    oracle.tr_loop(plan, states, target, steps, w.K,
+                   qkv=oracle_qkv(w, seqs) if (attn and w.attention) else None,
+                   scale=w.d ** -0.5, on_step=on_step, seqs=seqs)
+    return recs
+
+
+def test_tiny_loop_full_config():
+    """One sequence, 80-node tree, V=32000 int64, prefix 512, 64 steps, 32 heads."""
+    w = synth.WORKLOADS["tiny"]
+    recs = _check_loop(w, w.steps)
+    mat = np.mean([r["acc_len"][0] + 1 for r in recs])
+    assert mat > 1.5   # acceptance is nontrivial on this target
+
+
+def test_batched_reduced():
+    """Sequences with their own matrices and ragged prefixes (1k..4k)."""
+    w = synth.WORKLOADS["batched"].scaled(B=3, steps=10)
+    _check_loop(w, w.steps)
+
+
+def test_gqa_large_vocab_reduced():
+    """V=128256, int32 matrix, 128-node tree, bf16 logits, 32/8 grouped-query heads."""
+    w = synth.WORKLOADS["gqa"].scaled(B=2, steps=3)
+    _check_loop(w, w.steps)
+
+
+def test_long_context_reduced():
+    """Prefix 32768 (the full length), 128-node tree."""
+    w = synth.WORKLOADS["long"].scaled(B=1, steps=2)
+    _check_loop(w, w.steps)
+
+
+def test_lmhead_loop_reduced():
+    """Fused LM head (D=4096, V=32000) feeding accept and update."""
+    w = synth.WORKLOADS["lmhead"].scaled(B=3, steps=4)
+    _check_loop(w, w.steps, attn=False)
+
+
+def test_accepted_only_update_mode():
+    import free_speculative_decoding_gb300 as tr
+    from free_speculative_decoding_gb300.engine import TRState
+    from synth import device as sd
+    w = synth.WORKLOADS["tiny"].scaled(steps=6)
+    plan = oracle.TreePlan(w.child_counts, w.K)
+    tree = tr.Tree(w.child_counts, w.K)
+    st = TRState(tree, 1, w.V)
+    sd.warm_matrices(w, st)
+    st.start(synth.initial_roots(w), w.prefix_lengths(), M_src=st.M.clone())
+    tgt = sd.DeviceTarget(w, tree)
+    for _ in range(w.steps):
+        st.finish(logits=tgt.logits_for(st), mode=tr.TR_UPD_ACCEPTED)
+    ostate = oracle_states(w, [0], with_cache=False)
+    oracle.tr_loop(plan, ostate, target_fn(w), w.steps, w.K, mode=oracle.UPD_ACCEPTED)
+    assert np.array_equal(st.M[0].cpu().numpy(), ostate[0].M)
+    assert st.root.item() == ostate[0].root and st.L.item() == ostate[0].L
+
+
+# ----------------------------------------------------------------------------
+# full-size workloads, in the benchmark's launch configuration
+# ----------------------------------------------------------------------------
+
+def _greedy_ok(w, b, emitted, L0, root):
+    def top1(pos, x):
+        return int(np.argmax(synth.logits_f32(w.seed, b, pos, [x], w.V, w.logits)[0]))
+    return emitted == oracle.greedy_decode(top1, root, L0, len(emitted))
+
+
+def _emitted(recs, b):
+    out = []
+    for r in recs:
+        a = int(r["acc_len"][b])
+        out.extend(int(x) for x in r["committed"][b][:a + 1])
+    return out
+
+
+def test_batched_full_size_samples_and_losslessness():
+    """16 sequences x 256 steps: losslessness on sampled sequences, full integer
+    replay of one sequence over the first 48 steps, attention at step 0."""
+    w = synth.WORKLOADS["batched"]
+    b = 5
+    recs, st, status = run_gpu_loop(w, w.steps, keep_M_every=0, o_seqs=[b])
+    assert status == 0
+    L0, roots = w.prefix_lengths(), synth.initial_roots(w)
+    for bb in (0, 7, 15):
+        em = _emitted(recs, bb)
+        assert len(em) >= w.steps
+        assert _greedy_ok(w, bb, em, int(L0[bb]), int(roots[bb]))
+    plan = oracle.TreePlan(w.child_counts, w.K)
+    states = oracle_states(w, [b], with_cache=True)
+    steps = 48
+
+    def on_step(s, i, rec):
+        compare_step(w, plan, s, i, b, rec, recs[s], attn=True)
+
+    oracle.tr_loop(plan, states, target_fn(w), steps, w.K, qkv=oracle_qkv(w, [b]), scale=w.d ** -0.5,
+                   on_step=on_step, seqs=[b])
+    assert sum(int(r["acc_len"][b]) + 1 for r in recs[:steps]) == states[0].L - int(L0[b])
+
+
+def test_gqa_full_size_losslessness():
+    w = synth.WORKLOADS["gqa"].scaled(steps=24)
+    recs, st, status = run_gpu_loop(w, w.steps, keep_M_every=0, o_seqs=[3], o_steps={0})
+    assert status == 0
+    L0, roots = w.prefix_lengths(), synth.initial_roots(w)
+    for b in (0, 5):
+        assert _greedy_ok(w, b, _emitted(recs, b), int(L0[b]), int(roots[b]))
+    # attention of sampled nodes at step 0 in fp64
+    plan = oracle.TreePlan(w.child_counts, w.K)
+    st0 = oracle_states(w, [3], with_cache=True)[0]
+    q, kt, vt = synth.step_qkv(w, 0)
+    ref = oracle.tree_attention(synth.bf16_to_f32(q[3]), st0.kc, st0.vc, st0.L, synth.bf16_to_f32(kt[3]),
+                                synth.bf16_to_f32(vt[3]), plan, w.d ** -0.5)
+    assert rows_rel_err(recs[0]["O"][0], ref) <= ATTN_TOL
