@@ -62,6 +62,7 @@ _SIGS = {
     "tr_verify_attn_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _p]),
     "tr_topk": (_i, [_p, _i, _i64, _i64, _i64, _i, _p, _p, _p, _sz, _p]),
     "tr_topk_workspace_bytes": (_sz, [_i64, _i64, _i]),
+    "tr_topk_noalloc": (_i, [_p, _i, _i64, _i64, _i64, _i, _p, _p, _p]),
     "tr_lmhead_topk": (_i, [_p, _p, _i64, _i, _i64, _i, _p, _p, _p, _sz, _p]),
     "tr_lmhead_topk_workspace_bytes": (_sz, [_i64, _i, _i64, _i]),
     "tr_accept": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _p, _p]),
@@ -225,6 +226,21 @@ def tr_topk(logits, K, ids, vals, ws, V=None):
     _check("tr_topk", lib().tr_topk(_ptr(logits), _ftype(logits), rows, V, ld, K, _ptr(ids), _ptr(vals),
                                     _ptr(ws) if ws is not None else None, ws.numel() if ws is not None else 0,
                                     _stream()))
+
+
+TR_TOPK_NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def tr_topk_noalloc(logits, K, ids, vals, V=None):
+    """tr_topk without a workspace: the library's static device scratch is used.
+
+    For callers that cannot allocate device memory.  Calls on one device share
+    the scratch, so they must not overlap on the GPU."""
+    rows, ld = logits.shape
+    V = ld if V is None else V
+    _i32(ids, "ids")
+    _check("tr_topk_noalloc", lib().tr_topk_noalloc(_ptr(logits), _ftype(logits), rows, V, ld, K, _ptr(ids),
+                                                    _ptr(vals), _stream()))
 
 
 def tr_lmhead_topk_workspace_bytes(rows, D, V, K):

@@ -172,6 +172,28 @@ int tr_topk(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t
             int32_t *ids, float *vals, void *ws, size_t ws_bytes, tr_stream_t stream);
 size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K);
 
+/* Allocation-free variant of tr_topk (the paper has no counterpart; this is a
+ * library convenience).  For callers that hold logits, ids and vals on the
+ * device but cannot get more device memory: a plugin whose host framework owns
+ * every device buffer and gives plugins no workspace, a serving loop that must
+ * not call cudaMalloc (it can synchronise the device and stall every stream),
+ * or a foreign-function caller without an allocator.
+ * Same arguments and results as tr_topk, minus the workspace: the scratch
+ * lives in a static device array of TR_TOPK_NOALLOC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads it until the process exits.  Sizes
+ * whose scratch (tr_topk_workspace_bytes(rows, V, K)) exceeds that maximum are
+ * refused with TR_E_UNSUPPORTED before any launch.  The call allocates
+ * nothing: it clears the array's arrival counters with cudaMemsetAsync and
+ * launches the tr_topk kernel on the array.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array and it keeps the previous
+ * call's contents, so calls that overlap on the GPU (other streams, other
+ * host threads) race: serialise them on one stream. */
+#define TR_TOPK_NOALLOC_SCRATCH_BYTES (4u << 20)
+int tr_topk_noalloc(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K,
+                    int32_t *ids, float *vals, tr_stream_t stream);
+
 /* Fused LM head + top-K: logits = H . Wt^T (bf16 operands, fp32 accumulation)
  * and the top-K of each row as in tr_topk, without writing the logits.  The
  * distributions of the verified nodes come from the target's final
