@@ -480,6 +480,15 @@ def main():
         roofline = {"kernel": "tr_verify_attn", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                     "frac": ach / peak, "traffic": traffic, "peak_source": peak_kind,
                     "algorithmic_bytes_per_launch": a_bytes, "ms_per_launch": a_ms}
+    if wl.logits == "lmhead" and res["step_ms"]:
+        s_ms = float(np.mean(res["step_ms"]))
+        flops = 2.0 * wl.B * N * wl.D * wl.V
+        ach = flops / (s_ms * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        roofline = {"kernel": "tr_step (fused LM head + top-K, merge, accept/update)", "bound": "tensor",
+                    "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                    "peak_source": peak_kind + " bf16 dense (burst)", "flops_per_launch": flops,
+                    "ms_per_launch": s_ms}
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -7,12 +7,22 @@
 template <int KMAX>
 struct TopList {
   unsigned long long k[KMAX];
-  float thr;
+  float thr;    // values below thr cannot enter: max(own KMAX-th value, floor)
+  float floor;  // a value known to be beaten KMAX times elsewhere in the same merge group
 
   __device__ __forceinline__ void init() {
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) k[j] = 0ull;
     thr = -INFINITY;
+    floor = -INFINITY;
+  }
+
+  // Raise the rejection threshold to f, the KMAX-th best value of another list
+  // whose keys are merged with this one: a value strictly below f is beaten by
+  // KMAX keys of that list, so it cannot be among the merged top KMAX.
+  __device__ __forceinline__ void raise_floor(float f) {
+    floor = fmaxf(floor, f);
+    thr = fmaxf(thr, floor);
   }
 
   __device__ __forceinline__ void push(float v, uint32_t id) {
@@ -25,7 +35,7 @@ struct TopList {
           key = k[j] > key ? key : k[j];
           k[j] = hi;
         }
-        thr = k[KMAX - 1] ? tr_key_val(k[KMAX - 1]) : -INFINITY;
+        thr = fmaxf(k[KMAX - 1] ? tr_key_val(k[KMAX - 1]) : -INFINITY, floor);
       }
     }
   }

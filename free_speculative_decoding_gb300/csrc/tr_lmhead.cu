@@ -1,87 +1,193 @@
-// Fused LM head + top-K: logits = H . Wt^T never reach HBM; each
-// (row block, vocabulary tile) keeps only its rows' top-K keys, and a merge
-// kernel reduces the tiles' lists to the final top-K per row.
-#include "tr_internal.cuh"
+// Fused LM head + top-K on the 5th-generation tensor cores.
+//
+// logits = H . Wt^T (bf16 operands, fp32 accumulation) never reach HBM.  A
+// persistent kernel (one CTA per SM) walks 128 x 256 output tiles; per CTA:
+//   warp 0      TMA producer: 128x64 H and 256x64 Wt tiles, 128-byte swizzle,
+//               a 4-stage shared-memory ring guarded by mbarriers;
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//               one thread issues tcgen05.mma (M=128, N=256, K=16) per 16-wide
+//               K slice, committing each stage back to the producer and each
+//               finished tile to the epilogue;
+//   warps 2..5  epilogue: each thread owns one TMEM lane (one hidden row) and
+//               streams the tile's 256 fp32 logits from TMEM into a register
+//               top-K list, then writes that list (one per row and tile).
+// A second kernel merges each row's per-tile lists into the final top-K.  The
+// two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+//
+// Every mbarrier wait is bounded in time; a wait that gives up sets
+// TR_DEV_TIMEOUT, raises a block-wide abort flag, drains the copies and MMAs
+// already issued, frees TMEM and returns.
 #include "tr_lists.cuh"
+#include "tr_sm100.cuh"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kBM = 64;    // rows per tile
-constexpr int kBN = 128;   // vocabulary columns per tile
-constexpr int kBK = 32;    // reduction step
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int kThreads = 192;
+constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint32_t kIdesc = sm100::idesc_bf16_f32(BM, BN);
 
-// One 64 x 128 output tile on CUDA cores, fp32 accumulation of bf16 products,
-// followed by a per-row top-K of the tile written as KMAX keys per row.
+struct Bars {
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  uint32_t tmem;
+  int abort;
+};
+
 template <int KMAX>
-__global__ void __launch_bounds__(kThreads) lmhead_tile_kernel(const __nv_bfloat16 *H, const __nv_bfloat16 *Wt,
-                                                               long long rows, int D, long long V,
-                                                               unsigned long long *part, int n_vt) {
-  // operand tiles during the reduction, the output tile afterwards
-  constexpr int kOperands = kBK * (kBM + 1) + kBK * (kBN + 1);
-  constexpr int kOut = kBM * (kBN + 1);
-  __shared__ float buf[kOperands > kOut ? kOperands : kOut];
-  float (*Hs)[kBM + 1] = reinterpret_cast<float (*)[kBM + 1]>(buf);
-  float (*Ws)[kBN + 1] = reinterpret_cast<float (*)[kBN + 1]>(buf + kBK * (kBM + 1));
-  float (*Cs)[kBN + 1] = reinterpret_cast<float (*)[kBN + 1]>(buf);
-  const int tid = threadIdx.x;
-  const long long r0 = (long long)blockIdx.y * kBM;
-  const long long v0 = (long long)blockIdx.x * kBN;
-  // thread computes rows tr*4..+3 and columns tc + 16*j, j < 8
-  const int tr = tid >> 4, tc = tid & 15;
-  float acc[4][8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < D; k0 += kBK) {
-    for (int e = tid; e < kBM * kBK; e += kThreads) {
-      const int r = e / kBK, k = e % kBK;
-      const long long gr = r0 + r;
-      Hs[k][r] = gr < rows ? __bfloat162float(H[gr * D + k0 + k]) : 0.f;
+__global__ void __launch_bounds__(kThreads, 1)
+    lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int rows,
+                     long long V, int D, int n_mt, int n_nt, unsigned long long *part, unsigned *status) {
+  using namespace sm100;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Bars *bars = (Bars *)(smem + STAGES * STAGE_BYTES);
+  volatile int *abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = n_mt * n_nt;
+  const int nkb = D / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
     }
-    for (int e = tid; e < kBN * kBK; e += kThreads) {
-      const int v = e / kBK, k = e % kBK;
-      const long long gv = v0 + v;
-      Ws[k][v] = gv < V ? __bfloat162float(Wt[gv * D + k0 + k]) : 0.f;
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->tfull[a], 1);
+      mbar_init(&bars->tempty[a], 128);
     }
-    __syncthreads();
-#pragma unroll 8
-    for (int k = 0; k < kBK; ++k) {
-      float hv[4], wv[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) hv[i] = Hs[k][tr * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) wv[j] = Ws[k][tc + 16 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(hv[i], wv[j], acc[i][j]);
-    }
-    __syncthreads();
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) Cs[tr * 4 + i][tc + 16 * j] = acc[i][j];
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem, TMEM_COLS);
+  tc_fence_before();
   __syncthreads();
-  // per-row top-K of the tile: warp w takes rows w, w+8, ...
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int r = warp; r < kBM; r += kThreads / 32) {
-    const long long gr = r0 + r;
-    if (gr >= rows) break;
-    TopList<KMAX> L;
-    L.init();
-    for (int c = lane; c < kBN; c += 32) {
-      const long long gv = v0 + c;
-      if (gv < V) L.push(Cs[r][c], (uint32_t)gv);
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+
+  auto give_up = [&]() {
+    if (!*abort) {
+      *abort = 1;
+      tr_flag(status, TR_DEV_TIMEOUT);
     }
-    const unsigned long long mine = warp_merge<KMAX>(L, lane);
-    if (lane < KMAX) part[(gr * n_vt + blockIdx.x) * KMAX + lane] = mine;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      uint32_t armed_phase[STAGES];
+      bool armed[STAGES];
+      for (int s = 0; s < STAGES; ++s) armed[s] = false;
+      for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x) {
+        const int mt = t % n_mt, nt = t / n_mt;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&bars->empty[s], ph ^ 1, abort)) {
+            give_up();
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->full[s], STAGE_BYTES);
+          tma_load_2d(smem + s * STAGE_BYTES, &tmA, &bars->full[s], kb * BK, mt * BM);
+          tma_load_2d(smem + s * STAGE_BYTES + A_BYTES, &tmB, &bars->full[s], kb * BK, nt * BN);
+          armed[s] = true;
+          armed_phase[s] = ph;
+        }
+      }
+      if (*abort) {
+        // let the copies already issued land before the CTA can exit
+        for (int s = 0; s < STAGES; ++s)
+          if (armed[s]) mbar_drain(&bars->full[s], armed_phase[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int it = 0, tc = 0;
+      for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x, ++tc) {
+        const int acc = tc & 1;
+        const uint32_t aph = (tc >> 1) & 1;
+        if (!mbar_wait(&bars->tempty[acc], aph ^ 1, abort)) {
+          give_up();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1;
+          if (!mbar_wait(&bars->full[s], ph, abort)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(d, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), kIdesc,
+                     (kb | k) != 0 ? 1u : 0u);
+          mma_commit(&bars->empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&bars->tfull[acc]);
+      }
+      // every MMA issued so far completes before TMEM can be released
+      mma_commit(&bars->drain);
+      mbar_drain(&bars->drain, 0);
+    }
+  } else {
+    const int lane_base = (warp & 3) * 32;  // TMEM lanes this warp may read
+    int tc = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tc) {
+      const int mt = t % n_mt, nt = t / n_mt;
+      const int acc = tc & 1;
+      const uint32_t aph = (tc >> 1) & 1;
+      if (!mbar_wait(&bars->tfull[acc], aph, abort)) {
+        give_up();
+        break;
+      }
+      tc_fence_after();
+      TopList<KMAX> L;
+      L.init();
+      const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN);
+      const long long col0 = (long long)nt * BN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tmem_ld32(taddr + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const long long col = col0 + c0 + j;
+          if (col < V) L.push(v[j], (uint32_t)col);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->tempty[acc]);
+      const int row = mt * BM + lane_base + lane;
+      if (row < rows) {
+        unsigned long long *dst = part + ((long long)row * n_nt + nt) * KMAX;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) dst[j] = L.k[j];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
-// Final merge: one warp per row reduces n_vt lists of KMAX keys.
+// Final merge: one warp per row reduces n_lists lists of KMAX keys.
 template <int KMAX>
 __global__ void __launch_bounds__(128) merge_lists_kernel(const unsigned long long *part, long long rows, int n_lists,
                                                           int K, int32_t *ids, float *vals) {
@@ -105,42 +211,59 @@ __global__ void __launch_bounds__(128) merge_lists_kernel(const unsigned long lo
   }
 }
 
-int n_vtiles(long long V) { return (int)((V + kBN - 1) / kBN); }
+int n_ntiles(long long V) { return (int)((V + BN - 1) / BN); }
 
 template <int KMAX>
-void launch(const __nv_bfloat16 *H, const __nv_bfloat16 *Wt, long long rows, int D, long long V, int K, int32_t *ids,
-            float *vals, unsigned long long *part, cudaStream_t s) {
-  const int nvt = n_vtiles(V);
-  dim3 grid(nvt, (unsigned)((rows + kBM - 1) / kBM));
-  lmhead_tile_kernel<KMAX><<<grid, kThreads, 0, s>>>(H, Wt, rows, D, V, part, nvt);
-  merge_lists_kernel<KMAX><<<(unsigned)((rows + 3) / 4), 128, 0, s>>>(part, rows, nvt, K, ids, vals);
+int launch(const CUtensorMap &ta, const CUtensorMap &tb, long long rows, int D, long long V, int K, int32_t *ids,
+           float *vals, unsigned long long *part, cudaStream_t s) {
+  static bool attr_set[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(lmhead_tc_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+        cudaSuccess)
+      return TR_E_CUDA;
+    attr_set[dev] = true;
+  }
+  const int n_mt = (int)((rows + BM - 1) / BM), n_nt = n_ntiles(V);
+  const int tiles = n_mt * n_nt;
+  const int grid = tiles < tr_sm_count() ? tiles : tr_sm_count();
+  lmhead_tc_kernel<KMAX><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, (int)rows, V, D, n_mt, n_nt, part,
+                                                            tr_status_dev());
+  merge_lists_kernel<KMAX><<<(unsigned)((rows + 3) / 4), 128, 0, s>>>(part, rows, n_nt, K, ids, vals);
+  return TR_OK;
 }
 
 }  // namespace
 
 extern "C" size_t tr_lmhead_topk_workspace_bytes(int64_t rows, int D, int64_t V, int K) {
   if (rows <= 0 || D <= 0 || V <= 0 || K < 1 || K > TR_MAX_K) return 0;
-  return tr_align_up((size_t)rows * n_vtiles(V) * tr_kmax(K) * 8, 256);
+  return tr_align_up((size_t)rows * n_ntiles(V) * tr_kmax(K) * 8, 256);
 }
 
 extern "C" int tr_lmhead_topk(const void *H, const void *Wt, int64_t rows, int D, int64_t V, int K, int32_t *ids,
                               float *vals, void *ws, size_t ws_bytes, tr_stream_t stream) {
   if (rows < 0 || D < 1 || V < 1 || K < 1 || K > TR_MAX_K || K > V) return TR_E_INVAL;
-  if (D % 64) return TR_E_UNSUPPORTED;
-  if (V > INT32_MAX || rows > 65535LL * kBM) return TR_E_UNSUPPORTED;
+  if (D % BK) return TR_E_UNSUPPORTED;
+  if (V > INT32_MAX || rows > INT32_MAX / 2) return TR_E_UNSUPPORTED;
   if (rows == 0) return TR_OK;
   if (!H || !Wt || !ids) return TR_E_INVAL;
+  if (((uintptr_t)H | (uintptr_t)Wt) & 15) return TR_E_INVAL;
   if (!ws || ws_bytes < tr_lmhead_topk_workspace_bytes(rows, D, V, K)) return TR_E_INVAL;
   int rc = tr_check_device();
   if (rc != TR_OK) return rc;
+  CUtensorMap ta, tb;
+  rc = tr_make_tmap_2d_bf16(&ta, H, (uint64_t)D, (uint64_t)rows, (uint64_t)D * 2, BK, BM);
+  if (rc != TR_OK) return rc;
+  rc = tr_make_tmap_2d_bf16(&tb, Wt, (uint64_t)D, (uint64_t)V, (uint64_t)D * 2, BK, BN);
+  if (rc != TR_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   const int km = tr_kmax(K);
-  auto h = (const __nv_bfloat16 *)H;
-  auto w = (const __nv_bfloat16 *)Wt;
   auto part = (unsigned long long *)ws;
-  if (km == 8) launch<8>(h, w, rows, D, V, K, ids, vals, part, s);
-  else if (km == 16) launch<16>(h, w, rows, D, V, K, ids, vals, part, s);
-  else launch<32>(h, w, rows, D, V, K, ids, vals, part, s);
+  if (km == 8) rc = launch<8>(ta, tb, rows, D, V, K, ids, vals, part, s);
+  else if (km == 16) rc = launch<16>(ta, tb, rows, D, V, K, ids, vals, part, s);
+  else rc = launch<32>(ta, tb, rows, D, V, K, ids, vals, part, s);
+  if (rc != TR_OK) return rc;
   TR_LAUNCH_CHECK();
   return TR_OK;
 }

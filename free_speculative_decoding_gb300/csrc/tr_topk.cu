@@ -14,7 +14,7 @@
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kUnroll = 4;
 constexpr long long kChunk = 8192;  // target elements per CTA
 constexpr int kMaxSplits = 32;
@@ -73,18 +73,24 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long lo
     constexpr int kV = Elem<T>::kVec;
     const uint4 *xv = reinterpret_cast<const uint4 *>(x + lo);
     const int nvec = (int)((hi - lo) / kV);
-    for (int i0 = tid; i0 < nvec; i0 += kThreads * kUnroll) {
+    // warp-uniform trip count so the lanes can share their thresholds
+    for (int base = 0; base < nvec; base += kThreads * kUnroll) {
       uint4 buf[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int i = i0 + u * kThreads;
+        const int i = base + tid + u * kThreads;
         if (i < nvec) buf[u] = __ldcs(xv + i);
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int i = i0 + u * kThreads;
+        const int i = base + tid + u * kThreads;
         if (i < nvec) Elem<T>::template push_vec<KMAX>(L, buf[u], (uint32_t)(lo + (long long)i * kV));
       }
+      // the best KMAX-th value of any lane bounds what can still enter the warp's top KMAX
+      float f = L.k[KMAX - 1] ? tr_key_val(L.k[KMAX - 1]) : -INFINITY;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, off));
+      L.raise_floor(f);
     }
     done = lo + (long long)nvec * kV;
   }
