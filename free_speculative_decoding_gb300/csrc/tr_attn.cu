@@ -1,227 +1,596 @@
-// Tree-attention verification: split-KV decode over the prefix cache plus the
-// flattened draft tree, with the ancestor-only mask read from the tree plan.
+// Tree-attention verification on the 5th-generation tensor cores.
 //
-// The key space of sequence b is [0, L[b] + N): positions below L[b] come
-// from the cache, the rest are the tree nodes in BFS order.  It is cut into
-// chunks of kChunk keys; one CTA handles one (sequence, query head, chunk),
-// keeps an online softmax per tree node, and, when the sequence needs several
-// chunks, publishes (m, l, unnormalised O) partials that the last CTA of the
-// (sequence, head) to arrive merges (an arrival counter, no spin-wait).
-#include "tr_internal.cuh"
+// For node i and query head h (KV head g = h / (Hq/Hkv)) the output is the
+// softmax-weighted sum over the cached keys [0, L[b]) and the tree nodes on the
+// root-to-i path (blog "token-recycling", 完整工作流程 step 3; the
+// speculative-decoding lesson's tree attention).
+//
+// Work decomposition (stream-K): a "pair" is (sequence, KV head, group of MT
+// query heads); its keys are ceil(L/64) cache tiles of 64 keys followed by
+// ceil(N/64) tree tiles.  All pairs' tiles form one sequence that is cut into
+// equal contiguous ranges, one per CTA (one CTA per SM), so every SM streams
+// the same number of K/V bytes whatever the mix of prefix lengths.  A pair
+// that lies inside one range is finished in place; a pair cut by a range
+// boundary leaves (m, l, O) partials in two slots per CTA, and a small second
+// kernel merges them.
+//
+// Per CTA:
+//   warp 0      TMA producer: the pair's Q tile(s) (3-D map over [B*N, Hq, d]),
+//               then K and V tiles of 64 keys from the cache (2-D map over
+//               [B*Hkv*cap, d]) or the tree (3-D map over [B*N, Hkv, d]), all
+//               with the 128-byte swizzle, into separate K and V rings;
+//   warp 1      one thread issues tcgen05.mma: S = Q.K^T (M128 x N64 x K128,
+//               fp32 in TMEM, double-buffered) and O += P.V (M128 x N128 x K64,
+//               V read as an MN-major operand, O in TMEM across the segment);
+//   warps 2..   softmax, one query row per thread (one TMEM lane): the mask
+//               (key < L for the cache, ancestor bit for the tree), exp2 with a
+//               running maximum that only rescales O when it grows by more
+//               than 2^8, P written to shared memory in the swizzled K-major
+//               layout the next MMA reads.  P goes in two bf16 parts, hi =
+//               bf16(p) and lo = bf16(p - hi), both multiplied with V, so the
+//               weights reach the accumulator with ~2^-17 relative error
+//               instead of bf16's 2^-9.  At the end of a segment the same
+//               threads normalise O or write the partial.
+// MT query heads sharing one KV head are processed together (MT = 2 for
+// grouped-query attention), so every K/V tile feeds 128*MT query rows.
+//
+// Every mbarrier wait is bounded in time; a wait that gives up sets
+// TR_DEV_TIMEOUT and raises a block-wide abort flag; the roles drain their
+// in-flight copies and MMAs, TMEM is freed and the kernel returns.
+#include <algorithm>
+
+#include "tr_sm100.cuh"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kD = 128;       // head dimension
-constexpr int kTile = 64;     // keys per tile
-constexpr int kChunk = 1024;  // keys per CTA
-constexpr int kKStride = kD + 1;
+constexpr int kD = 128;             // head dimension
+constexpr int BN = 64;              // keys per tile
+constexpr float kRescaleLog2 = 8.f; // O is rescaled only when the row maximum grows by more than this
+constexpr int kMaxB = 1024;
+
+template <int MT>
+struct Cfg {
+  static constexpr int STAGES = MT == 1 ? 3 : 2;
+  static constexpr int PB = MT == 1 ? 2 : 1;      // P buffers (hi + lo parts each)
+  static constexpr int Q_HALF = 128 * 128;        // 128 rows x 64 bf16 (one d-half), bytes
+  static constexpr int KV_HALF = 64 * 128;        // 64 keys x 64 bf16
+  static constexpr int KV_TILE = 2 * KV_HALF;
+  static constexpr int P_PART = 128 * 128;        // 128 rows x 64 keys x 2 B
+  static constexpr int P_TILE = 2 * P_PART;       // hi, lo
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + MT * 2 * Q_HALF;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
+  static constexpr int OFF_P = OFF_V + STAGES * KV_TILE;
+  static constexpr int OFF_BAR = OFF_P + PB * MT * P_TILE;
+  static constexpr int THREADS = 64 + 128 * MT;
+  static constexpr int SOFT = 128 * MT;
+  static constexpr uint32_t TMEM_COLS = 256 * MT;
+  __host__ __device__ static constexpr uint32_t s_col(int buf, int m) { return (uint32_t)((buf * MT + m) * BN); }
+  __host__ __device__ static constexpr uint32_t o_col(int m) { return (uint32_t)(2 * MT * BN + m * kD); }
+};
+
+template <int S, int PB>
+struct Bars {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[S], k_empty[S], v_full[S], v_empty[S];
+  uint64_t s_full[2], p_full[PB], pv_done[PB];
+  uint64_t o_full, o_empty, drain;
+  uint32_t tmem;
+  int abort;
+  int Ls[kMaxB];
+  int pref[kMaxB + 1];  // first tile of sequence b in the global tile order
+};
 
 struct AttnArgs {
-  const __nv_bfloat16 *Q, *Kt, *Vt, *Kc, *Vc;
   const int32_t *L;
   float *O;
-  float *part_o;     // [B*Hq, CH, N, D]
-  float2 *part_ml;   // [B*Hq, CH, N]
-  unsigned *counters;  // [B*Hq]
-  int cap, B, Hq, Hkv, CH;
-  float scale;
+  float *part_o;      // [grid, 2, MT, N, d]
+  float2 *part_ml;    // [grid, 2, MT, N]
   unsigned *status;
+  int B, N, Hq, Hkv, G, HG, cap;
+  int q_rows, c_rows, t_rows;  // TMA box heights (at most the tensor's extent)
+  float scale_log2;
 };
 
-__device__ __forceinline__ float bf(const __nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ int tiles_per_pair(int Lb, int N) { return (Lb + BN - 1) / BN + (N + BN - 1) / BN; }
 
-__global__ void __launch_bounds__(kThreads) attn_kernel(AttnArgs a, const __grid_constant__ TreeDev tree) {
-  extern __shared__ float smem[];
-  const int N = tree.N;
-  float *Qs = smem;                          // [N][kD]
-  float *Ks = Qs + TR_MAX_NODES * kD;        // [kTile][kKStride]
-  float *Vs = Ks + kTile * kKStride;         // [kTile][kD]
-  float *Ss = Vs + kTile * kD;               // [N][kTile]
-  float *ms = Ss + TR_MAX_NODES * kTile;     // [N]
-  float *ls = ms + TR_MAX_NODES;             // [N]
-  float *cs = ls + TR_MAX_NODES;             // [N]
-  __shared__ int is_last;
+// Range of global tiles owned by CTA c of `grid`.
+__device__ __forceinline__ long long range_start(long long total, int c, int grid) { return total * c / grid; }
 
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
-  const int g = h / (a.Hq / a.Hkv);
-  int Lb = a.L[b];
-  if (Lb < 0 || Lb > a.cap) {
-    if (tid == 0 && c == 0) tr_flag(a.status, TR_DEV_BAD_LENGTH);
-    Lb = Lb < 0 ? 0 : a.cap;
-  }
-  const int total = Lb + N;
-  const int nch = (total + kChunk - 1) / kChunk;
-  if (c >= nch) return;
-  const int k_lo = c * kChunk, k_hi = min(total, k_lo + kChunk);
+// A run of consecutive tiles of one pair inside one CTA's range.
+struct Seg {
+  int b, g, hg, pair, Lb;
+  int j0, n;    // first tile within the pair, number of tiles
+  int n_ct;     // cache tiles of the pair
+  bool complete, first_of_cta;
+};
 
-  // queries of this head for every node
-  for (int e = tid; e < N * kD; e += kThreads) {
-    const int n = e / kD, i = e % kD;
-    Qs[n * kD + i] = bf(a.Q[(((long long)b * N + n) * a.Hq + h) * kD + i]);
+__device__ __forceinline__ Seg decode(long long t, long long t_lo, long long t_hi, const int *pref, const int *Ls,
+                                      const AttnArgs &a) {
+  int lo = 0, hi = a.B - 1;  // largest b with pref[b] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= t) lo = mid;
+    else hi = mid - 1;
   }
-  for (int n = tid; n < N; n += kThreads) {
-    ms[n] = -INFINITY;
-    ls[n] = 0.f;
-  }
-  // O accumulators: thread owns column i = tid % 128 of rows tid/128 + 2r
-  const int oi = tid & (kD - 1), orow0 = tid >> 7;
-  float acc[TR_MAX_NODES / 2];
-#pragma unroll
-  for (int r = 0; r < TR_MAX_NODES / 2; ++r) acc[r] = 0.f;
-  __syncthreads();
-
-  const long long cache_base = ((long long)b * a.Hkv + g) * a.cap;
-  for (int t0 = k_lo; t0 < k_hi; t0 += kTile) {
-    // stage K and V of keys [t0, t0 + kTile)
-    for (int e = tid; e < kTile * kD; e += kThreads) {
-      const int j = e / kD, i = e % kD;
-      const int key = t0 + j;
-      float kv = 0.f, vv = 0.f;
-      if (key < k_hi) {
-        if (key < Lb) {
-          kv = bf(a.Kc[(cache_base + key) * kD + i]);
-          vv = bf(a.Vc[(cache_base + key) * kD + i]);
-        } else {
-          const int node = key - Lb;
-          kv = bf(a.Kt[(((long long)b * N + node) * a.Hkv + g) * kD + i]);
-          vv = bf(a.Vt[(((long long)b * N + node) * a.Hkv + g) * kD + i]);
-        }
-      }
-      Ks[j * kKStride + i] = kv;
-      Vs[j * kD + i] = vv;
-    }
-    __syncthreads();
-    // scores: thread owns key j = tid % 64 for rows tid/64 + 4r
-    {
-      const int j = tid & (kTile - 1), r0 = tid >> 6;
-      const int key = t0 + j;
-      float s[TR_MAX_NODES / 4];
-#pragma unroll
-      for (int r = 0; r < TR_MAX_NODES / 4; ++r) s[r] = 0.f;
-      for (int i = 0; i < kD; ++i) {
-        const float kk = Ks[j * kKStride + i];
-#pragma unroll
-        for (int r = 0; r < TR_MAX_NODES / 4; ++r) {
-          const int n = r0 + 4 * r;
-          if (n < N) s[r] = fmaf(Qs[n * kD + i], kk, s[r]);
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < TR_MAX_NODES / 4; ++r) {
-        const int n = r0 + 4 * r;
-        if (n < N) {
-          bool vis = key < k_hi;
-          if (vis && key >= Lb) {
-            const int node = key - Lb;
-            vis = (tree.anc[n][node >> 6] >> (node & 63)) & 1ull;
-          }
-          Ss[n * kTile + j] = vis ? s[r] * a.scale : -INFINITY;
-        }
-      }
-    }
-    __syncthreads();
-    // online softmax per row
-    for (int n = tid; n < N; n += kThreads) {
-      float mx = -INFINITY;
-      for (int j = 0; j < kTile; ++j) mx = fmaxf(mx, Ss[n * kTile + j]);
-      const float m_old = ms[n];
-      const float m_new = fmaxf(m_old, mx);
-      float corr = 1.f, sum = 0.f;
-      if (m_new != -INFINITY) {
-        corr = m_old == -INFINITY ? 0.f : expf(m_old - m_new);
-        for (int j = 0; j < kTile; ++j) {
-          const float sv = Ss[n * kTile + j];
-          const float p = sv == -INFINITY ? 0.f : expf(sv - m_new);
-          Ss[n * kTile + j] = p;
-          sum += p;
-        }
-      } else {
-        for (int j = 0; j < kTile; ++j) Ss[n * kTile + j] = 0.f;
-      }
-      ms[n] = m_new;
-      ls[n] = ls[n] * corr + sum;
-      cs[n] = corr;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < TR_MAX_NODES / 2; ++r) {
-      const int n = orow0 + 2 * r;
-      if (n < N) {
-        float o = acc[r] * cs[n];
-        for (int j = 0; j < kTile; ++j) o = fmaf(Ss[n * kTile + j], Vs[j * kD + oi], o);
-        acc[r] = o;
-      }
-    }
-    __syncthreads();
-  }
-
-  const long long bh = (long long)b * a.Hq + h;
-  if (nch == 1) {
-#pragma unroll
-    for (int r = 0; r < TR_MAX_NODES / 2; ++r) {
-      const int n = orow0 + 2 * r;
-      if (n < N) a.O[(((long long)b * N + n) * a.Hq + h) * kD + oi] = acc[r] / ls[n];
-    }
-    return;
-  }
-  // publish the partial of this chunk
-  float *po = a.part_o + (bh * a.CH + c) * (long long)N * kD;
-#pragma unroll
-  for (int r = 0; r < TR_MAX_NODES / 2; ++r) {
-    const int n = orow0 + 2 * r;
-    if (n < N) po[n * kD + oi] = acc[r];
-  }
-  for (int n = tid; n < N; n += kThreads) a.part_ml[(bh * a.CH + c) * N + n] = make_float2(ms[n], ls[n]);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) is_last = atomicAdd(&a.counters[bh], 1u) == (unsigned)(nch - 1);
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // merge the chunks of this (sequence, head)
-  for (int e = tid; e < N * kD; e += kThreads) {
-    const int n = e / kD, i = e % kD;
-    float M = -INFINITY;
-    for (int q = 0; q < nch; ++q) M = fmaxf(M, __ldcg(&a.part_ml[(bh * a.CH + q) * N + n].x));
-    float num = 0.f, den = 0.f;
-    for (int q = 0; q < nch; ++q) {
-      const float2 ml = __ldcg(&a.part_ml[(bh * a.CH + q) * N + n]);
-      const float w = ml.x == -INFINITY ? 0.f : expf(ml.x - M);
-      den += ml.y * w;
-      num += __ldcg(&a.part_o[((bh * a.CH + q) * N + n) * (long long)kD + i]) * w;
-    }
-    a.O[(((long long)b * N + n) * a.Hq + h) * kD + i] = num / den;
-  }
-  if (tid == 0) a.counters[bh] = 0u;
+  Seg s;
+  s.b = lo;
+  s.Lb = Ls[lo];
+  const int tpp = tiles_per_pair(s.Lb, a.N);
+  const long long r = t - pref[lo];
+  const int pib = (int)(r / tpp);
+  s.j0 = (int)(r % tpp);
+  s.g = pib / a.HG;
+  s.hg = pib % a.HG;
+  s.pair = (s.b * a.Hkv + s.g) * a.HG + s.hg;
+  s.n = (int)min((long long)(tpp - s.j0), t_hi - t);
+  s.n_ct = (s.Lb + BN - 1) / BN;
+  s.complete = s.j0 == 0 && s.n == tpp;
+  s.first_of_cta = t == t_lo;
+  return s;
 }
 
-constexpr size_t kSmemBytes =
-    sizeof(float) * (TR_MAX_NODES * kD + kTile * kKStride + kTile * kD + TR_MAX_NODES * kTile + 3 * TR_MAX_NODES);
+template <int MT>
+__global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKc,
+                   const __grid_constant__ CUtensorMap tmVc, const __grid_constant__ CUtensorMap tmKt,
+                   const __grid_constant__ CUtensorMap tmVt, const AttnArgs a, const __grid_constant__ TreeDev tree) {
+  using namespace sm100;
+  using C = Cfg<MT>;
+  constexpr int S = C::STAGES, PB = C::PB;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Bars<S, PB> *bars = (Bars<S, PB> *)(smem + C::OFF_BAR);
+  volatile int *abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
 
-int max_chunks(int cap, int N) { return (cap + N + kChunk - 1) / kChunk; }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) mbar_init(&bars->s_full[b], 1);
+    for (int b = 0; b < PB; ++b) {
+      mbar_init(&bars->p_full[b], C::SOFT);
+      mbar_init(&bars->pv_done[b], 1);
+    }
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_empty, C::SOFT);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
+    int Lb = a.L[b];
+    if (Lb < 0 || Lb > a.cap) {
+      if (blockIdx.x == 0) tr_flag(a.status, TR_DEV_BAD_LENGTH);
+      Lb = Lb < 0 ? 0 : a.cap;
+    }
+    bars->Ls[b] = Lb;
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = 0; b < a.B; ++b) {
+      bars->pref[b] = acc;
+      acc += tiles_per_pair(bars->Ls[b], N) * a.Hkv * a.HG;
+    }
+    bars->pref[a.B] = acc;
+  }
+  __syncthreads();
+  const uint32_t tmem = bars->tmem;
+  const long long total = bars->pref[a.B];
+  const long long t_lo = range_start(total, blockIdx.x, gridDim.x);
+  const long long t_hi = range_start(total, blockIdx.x + 1, gridDim.x);
 
-struct WsLayout {
-  size_t o_off, ml_off, cnt_off, total;
+  auto give_up = [&]() {
+    if (!*abort) {
+      *abort = 1;
+      tr_flag(a.status, TR_DEV_TIMEOUT);
+    }
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmKc);
+      tma_prefetch_desc(&tmVc);
+      tma_prefetch_desc(&tmKt);
+      tma_prefetch_desc(&tmVt);
+      int kc = 0, vc = 0, sc = 0;
+      int q_armed = -1, k_last[S], v_last[S];
+      for (int s = 0; s < S; ++s) k_last[s] = v_last[s] = -1;
+      bool ok = true;
+      for (long long t = t_lo; t < t_hi && ok && !*abort; ++sc) {
+        const Seg sg = decode(t, t_lo, t_hi, bars->pref, bars->Ls, a);
+        t += sg.n;
+        if (!mbar_wait(&bars->q_empty, (sc & 1) ^ 1, abort)) {
+          give_up();
+          break;
+        }
+        mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(MT * 2 * a.q_rows * 128));
+        for (int m = 0; m < MT; ++m) {
+          const int h = sg.g * a.G + sg.hg * MT + m;
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(smem + C::OFF_Q + (m * 2 + half) * C::Q_HALF, &tmQ, &bars->q_full, half * 64, h, sg.b * N);
+        }
+        q_armed = sc & 1;
+        for (int u = 0; u < sg.n && ok; ++u) {
+          const int j = sg.j0 + u;
+          const bool cache = j < sg.n_ct;
+          const int y_cache = (sg.b * a.Hkv + sg.g) * a.cap + j * BN;
+          const int node0 = (j - sg.n_ct) * BN;
+          for (int kv = 0; kv < 2; ++kv) {
+            int &cnt = kv ? vc : kc;
+            uint64_t *full = kv ? bars->v_full : bars->k_full;
+            uint64_t *empty = kv ? bars->v_empty : bars->k_empty;
+            int *last = kv ? v_last : k_last;
+            const int s = cnt % S;
+            const uint32_t ph = (cnt / S) & 1;
+            if (!mbar_wait(&empty[s], ph ^ 1, abort)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * (cache ? a.c_rows : a.t_rows) * 128));
+            uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_TILE;
+            for (int half = 0; half < 2; ++half) {
+              if (cache)
+                tma_load_2d(dst + half * C::KV_HALF, kv ? &tmVc : &tmKc, &full[s], half * 64, y_cache);
+              else
+                tma_load_3d(dst + half * C::KV_HALF, kv ? &tmVt : &tmKt, &full[s], half * 64, sg.g,
+                            sg.b * N + node0);
+            }
+            last[s] = (int)ph;
+            ++cnt;
+          }
+        }
+      }
+      if (*abort) {
+        // let the copies already issued land before the CTA can exit
+        if (q_armed >= 0) mbar_drain(&bars->q_full, (uint32_t)q_armed);
+        for (int s = 0; s < S; ++s) {
+          if (k_last[s] >= 0) mbar_drain(&bars->k_full[s], (uint32_t)k_last[s]);
+          if (v_last[s] >= 0) mbar_drain(&bars->v_full[s], (uint32_t)v_last[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BN);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kD, true);
+      int kc = 0, vc = 0, gt = 0, sc = 0;
+      bool ok = true;
+      for (long long t = t_lo; t < t_hi && ok && !*abort; ++sc) {
+        const Seg sg = decode(t, t_lo, t_hi, bars->pref, bars->Ls, a);
+        t += sg.n;
+        const int T = sg.n;
+        if (!mbar_wait(&bars->q_full, sc & 1, abort)) {
+          give_up();
+          break;
+        }
+        tc_fence_after();
+        for (int u = 0; u <= T && ok; ++u) {
+          if (u < T) {
+            const int s = kc % S;
+            if (!mbar_wait(&bars->k_full[s], (kc / S) & 1, abort)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const int sb = (gt + u) & 1;
+            const uint32_t kb = smem_u32(smem + C::OFF_K + s * C::KV_TILE);
+            for (int m = 0; m < MT; ++m) {
+              const uint32_t qb = smem_u32(smem + C::OFF_Q + m * 2 * C::Q_HALF);
+#pragma unroll
+              for (int ks = 0; ks < kD / 16; ++ks)
+                mma_bf16(tmem + C::s_col(sb, m), desc_kmajor_sw128(qb + (ks >> 2) * C::Q_HALF + (ks & 3) * 32),
+                         desc_kmajor_sw128(kb + (ks >> 2) * C::KV_HALF + (ks & 3) * 32), kIdescQK, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->k_empty[s]);
+            mma_commit(&bars->s_full[sb]);
+            if (u == T - 1) mma_commit(&bars->q_empty);
+            ++kc;
+          }
+          if (u >= 1) {
+            const int j = u - 1, gj = gt + j, pb = gj % PB;
+            if (!mbar_wait(&bars->p_full[pb], (gj / PB) & 1, abort)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            const int s = vc % S;
+            if (!mbar_wait(&bars->v_full[s], (vc / S) & 1, abort)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            if (j == 0 && !mbar_wait(&bars->o_empty, (sc & 1) ^ 1, abort)) {
+              give_up();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t vb = smem_u32(smem + C::OFF_V + s * C::KV_TILE);
+            for (int m = 0; m < MT; ++m) {
+              const uint32_t pbase = smem_u32(smem + C::OFF_P + (pb * MT + m) * C::P_TILE);
+#pragma unroll
+              for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int ks = 0; ks < BN / 16; ++ks)
+                  mma_bf16(tmem + C::o_col(m), desc_kmajor_sw128(pbase + part * C::P_PART + ks * 32),
+                           desc_mnmajor_sw128(vb + ks * 2048, C::KV_HALF), kIdescPV,
+                           (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->v_empty[s]);
+            mma_commit(&bars->pv_done[pb]);
+            ++vc;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bars->o_full);
+        gt += T;
+      }
+      mma_commit(&bars->drain);
+      mbar_drain(&bars->drain, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int mt = (warp - 2) >> 2;
+    const int quad = warp & 3;  // TMEM lanes quad*32 .. +31
+    const int r = quad * 32 + lane;
+    const bool warp_active = quad * 32 < N;
+    const bool row_valid = r < N;
+    const int rn = row_valid ? r : 0;
+    const unsigned long long anc0 = tree.anc[rn][0], anc1 = tree.anc[rn][1];
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    uint8_t *prow_base = smem + C::OFF_P + mt * C::P_TILE + (r >> 3) * 1024 + (r & 7) * 128;
+    // every wait of this role is warp-uniform: a lane that gives up takes its
+    // whole warp with it, so the warp-collective TMEM accesses stay converged
+    auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      const bool mine = mbar_wait(bar, parity, abort);
+      const bool all = __all_sync(0xffffffffu, mine);
+      if (!all) give_up();
+      return all;
+    };
+    int gt = 0, sc = 0;
+    bool ok = true;
+    for (long long t = t_lo; t < t_hi && ok; ++sc) {
+      const Seg sg = decode(t, t_lo, t_hi, bars->pref, bars->Ls, a);
+      t += sg.n;
+      const int T = sg.n;
+      const int h = sg.g * a.G + sg.hg * MT + mt;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int u = 0; u < T && ok; ++u) {
+        const int gtt = gt + u, sb = gtt & 1, pb = gtt % PB;
+        if (!wwait(&bars->s_full[sb], (gtt >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (warp_active) {
+          float sv[BN];
+          {
+            float tmp[32];
+            tmem_ld32(tmem + lane_off + C::s_col(sb, mt), tmp);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sv[c] = tmp[c];
+            tmem_ld32(tmem + lane_off + C::s_col(sb, mt) + 32, tmp);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) sv[32 + c] = tmp[c];
+          }
+          const int j = sg.j0 + u;
+          const bool cache = j < sg.n_ct;
+          const int key0 = j * BN;
+          const int node0 = (j - sg.n_ct) * BN;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < BN; ++c) {
+            bool valid;
+            if (cache) {
+              valid = key0 + c < sg.Lb;
+            } else {
+              const int nd = node0 + c;
+              const unsigned long long w = nd < 64 ? anc0 : anc1;
+              valid = nd < N && ((w >> (nd & 63)) & 1ull);
+            }
+            valid = valid && row_valid;
+            sv[c] = valid ? sv[c] * a.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, sv[c]);
+          }
+          const float m_new = fmaxf(m_run, mx);
+          const bool need = m_new > m_run + kRescaleLog2;  // also true for the row's first finite maximum
+          if (__any_sync(0xffffffffu, need && u > 0)) {
+            // O already holds earlier tiles: wait for the last PV, then scale O in TMEM
+            const int gp = gtt - 1;
+            if (!wwait(&bars->pv_done[gp % PB], (gp / PB) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float f = (need && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+              float ov[32];
+              tmem_ld32(tmem + lane_off + C::o_col(mt) + c0, ov);
+#pragma unroll
+              for (int c = 0; c < 32; ++c) ov[c] *= f;
+              tmem_st32(tmem + lane_off + C::o_col(mt) + c0, ov);
+            }
+          }
+          if (need) {
+            l_run = m_run == -INFINITY ? 0.f : l_run * ex2(m_run - m_new);
+            m_run = m_new;
+          }
+          // this P buffer is free once the PV that last read it is done
+          if (gtt >= PB && !wwait(&bars->pv_done[pb], ((gtt - PB) / PB) & 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t *prow = prow_base + pb * MT * C::P_TILE;
+#pragma unroll
+          for (int c8 = 0; c8 < BN / 8; ++c8) {
+            uint32_t whi[4], wlo[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float x0 = sv[c8 * 8 + 2 * q], x1 = sv[c8 * 8 + 2 * q + 1];
+              const float p0 = x0 == -INFINITY ? 0.f : ex2(x0 - m_run);
+              const float p1 = x1 == -INFINITY ? 0.f : ex2(x1 - m_run);
+              l_run += p0 + p1;
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(hi), p1 - __high2float(hi));
+              whi[q] = *reinterpret_cast<const uint32_t *>(&hi);
+              wlo[q] = *reinterpret_cast<const uint32_t *>(&lo);
+            }
+            const int off = (c8 ^ (r & 7)) << 4;
+            *reinterpret_cast<uint4 *>(prow + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+            *reinterpret_cast<uint4 *>(prow + C::P_PART + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[pb]);
+      }
+      if (!ok) break;
+      // ---- end of the segment: normalised output or a partial
+      if (!wwait(&bars->o_full, sc & 1)) break;
+      tc_fence_after();
+      if (warp_active) {
+        const int slot = blockIdx.x * 2 + (sg.first_of_cta ? 0 : 1);
+        const long long prow_idx = ((long long)slot * MT + mt) * N + r;
+        const float inv = row_valid && l_run > 0.f ? 1.f / l_run : 0.f;
+        float *dst = sg.complete ? a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD : a.part_o + prow_idx * kD;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          float ov[32];
+          tmem_ld32(tmem + lane_off + C::o_col(mt) + c0, ov);
+          if (row_valid) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4) {
+              const float4 v4 = sg.complete
+                                    ? make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv)
+                                    : make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
+              *reinterpret_cast<float4 *>(dst + c0 + c) = v4;
+            }
+          }
+        }
+        if (!sg.complete && row_valid) a.part_ml[prow_idx] = make_float2(m_run, l_run);
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_empty);
+      gt += T;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// Merges the partials of every pair that two or more CTAs shared.  One block
+// per (pair, query head of the group), one thread per tree node.
+__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a, int MT, int grid) {
+  __shared__ int pref_s[kMaxB + 1];
+  __shared__ int Ls[kMaxB];
+  const int pair = blockIdx.x, m = blockIdx.y;
+  for (int b = threadIdx.x; b < a.B; b += blockDim.x) Ls[b] = min(max(a.L[b], 0), a.cap);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = 0; b < a.B; ++b) {
+      pref_s[b] = acc;
+      acc += tiles_per_pair(Ls[b], a.N) * a.Hkv * a.HG;
+    }
+    pref_s[a.B] = acc;
+  }
+  __syncthreads();
+  const int b = pair / (a.Hkv * a.HG), pib = pair % (a.Hkv * a.HG);
+  const int g = pib / a.HG, hg = pib % a.HG;
+  const long long total = pref_s[a.B];
+  const int tpp = tiles_per_pair(Ls[b], a.N);
+  const long long first = pref_s[b] + (long long)pib * tpp, last = first + tpp - 1;
+  // CTA c owns [total*c/grid, total*(c+1)/grid): the owner of tile t is ceil((t+1)*grid/total) - 1
+  const int c0 = (int)(((first + 1) * grid + total - 1) / total - 1);
+  const int c1 = (int)(((last + 1) * grid + total - 1) / total - 1);
+  if (c0 == c1) return;  // finished in place
+  const int n = threadIdx.x;
+  if (n >= a.N) return;
+  const int slot0 = c0 * 2 + (range_start(total, c0, grid) < first ? 1 : 0);
+  float M = -INFINITY;
+  for (int c = c0; c <= c1; ++c) {
+    const int slot = c == c0 ? slot0 : c * 2;
+    M = fmaxf(M, a.part_ml[((long long)slot * MT + m) * a.N + n].x);
+  }
+  float acc[kD];
+#pragma unroll
+  for (int i = 0; i < kD; ++i) acc[i] = 0.f;
+  float den = 0.f;
+  for (int c = c0; c <= c1; ++c) {
+    const int slot = c == c0 ? slot0 : c * 2;
+    const long long row = ((long long)slot * MT + m) * a.N + n;
+    const float2 ml = a.part_ml[row];
+    const float w = ml.x == -INFINITY ? 0.f : sm100::ex2(ml.x - M);
+    den += ml.y * w;
+    const float4 *src = reinterpret_cast<const float4 *>(a.part_o + row * kD);
+#pragma unroll
+    for (int i = 0; i < kD / 4; ++i) {
+      const float4 v = src[i];
+      acc[4 * i] += v.x * w;
+      acc[4 * i + 1] += v.y * w;
+      acc[4 * i + 2] += v.z * w;
+      acc[4 * i + 3] += v.w * w;
+    }
+  }
+  const float inv = 1.f / den;
+  const int h = g * a.G + hg * MT + m;
+  float4 *dst = reinterpret_cast<float4 *>(a.O + (((long long)b * a.N + n) * a.Hq + h) * kD);
+#pragma unroll
+  for (int i = 0; i < kD / 4; ++i)
+    dst[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+}
+
+template <int MT>
+size_t smem_bytes() {
+  return (size_t)Cfg<MT>::OFF_BAR + sizeof(Bars<Cfg<MT>::STAGES, Cfg<MT>::PB>) + 1024;
+}
+
+struct Plan {
+  int G, MT, HG, pairs, grid;
+  size_t o_off, ml_off, total;
 };
 
-WsLayout ws_layout(int B, int Hq, int cap, int N) {
-  WsLayout w;
-  const size_t CH = (size_t)max_chunks(cap, N);
-  const size_t bh = (size_t)B * Hq;
-  w.o_off = 0;
-  w.ml_off = tr_align_up(bh * CH * N * kD * sizeof(float), 256);
-  w.cnt_off = w.ml_off + tr_align_up(bh * CH * N * sizeof(float2), 256);
-  w.total = w.cnt_off + tr_align_up(bh * sizeof(unsigned), 256);
-  return w;
+Plan make_plan(int B, int Hq, int Hkv, int N) {
+  Plan p;
+  p.G = Hq / Hkv;
+  p.MT = p.G % 2 == 0 ? 2 : 1;
+  p.HG = p.G / p.MT;
+  p.pairs = B * Hkv * p.HG;
+  p.grid = tr_sm_count();
+  const size_t rows = (size_t)p.grid * 2 * p.MT * N;
+  p.o_off = 0;
+  p.ml_off = tr_align_up(rows * kD * sizeof(float), 256);
+  p.total = p.ml_off + tr_align_up(rows * sizeof(float2), 256);
+  return p;
 }
 
 }  // namespace
 
 extern "C" size_t tr_verify_attn_workspace_bytes(int B, int Hq, int Hkv, int d, int cap, const struct tr_tree *tree) {
-  if (!tree || B < 1 || Hq < 1 || Hkv < 1 || d != kD || cap < 0) return 0;
-  return ws_layout(B, Hq, cap, tree->dev.N).total;
+  if (!tree || B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || d != kD || cap < 0) return 0;
+  return make_plan(B, Hq, Hkv, tree->dev.N).total;
 }
 
 extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, const void *Kc, const void *Vc,
@@ -230,41 +599,75 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
   if (!Q || !Kt || !Vt || !Kc || !Vc || !L || !tree || !O || B < 1 || Hq < 1 || Hkv < 1 || cap < 0) return TR_E_INVAL;
   if (Hq % Hkv) return TR_E_INVAL;
   if (d != kD) return TR_E_UNSUPPORTED;
-  if (B > 65535 || Hq > 65535) return TR_E_UNSUPPORTED;
   const int N = tree->dev.N;
-  const WsLayout w = ws_layout(B, Hq, cap, N);
-  if (!ws || ws_bytes < w.total) return TR_E_INVAL;
+  // the global tile count must fit in 31 bits
+  const long long max_tiles = (long long)B * Hkv * Hq * ((cap + BN - 1) / BN + (N + BN - 1) / BN);
+  if (B > kMaxB || max_tiles >= (1LL << 31) || (long long)B * Hkv * cap >= (1LL << 31)) return TR_E_UNSUPPORTED;
+  const Plan p = make_plan(B, Hq, Hkv, N);
+  if (!ws || ws_bytes < p.total) return TR_E_INVAL;
   if (((uintptr_t)Q | (uintptr_t)Kt | (uintptr_t)Vt | (uintptr_t)Kc | (uintptr_t)Vc | (uintptr_t)O) & 15)
     return TR_E_INVAL;
   int rc = tr_check_device();
   if (rc != TR_OK) return rc;
-  static bool attr_set[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    TR_TRY_CUDA(cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
-    attr_set[dev] = true;
+
+  const uint32_t q_rows = (uint32_t)std::min<long long>(128, (long long)B * N);
+  const uint32_t c_rows = (uint32_t)std::min<long long>(BN, (long long)B * Hkv * (cap > 0 ? cap : 1));
+  const uint32_t t_rows = (uint32_t)std::min<long long>(BN, (long long)B * N);
+  CUtensorMap tq, tkc, tvc, tkt, tvt;
+  {
+    const uint64_t dq[3] = {(uint64_t)kD, (uint64_t)Hq, (uint64_t)B * N};
+    const uint64_t sq[2] = {(uint64_t)kD * 2, (uint64_t)Hq * kD * 2};
+    const uint32_t bq[3] = {64, 1, q_rows};
+    if ((rc = tr_make_tmap_bf16(&tq, Q, 3, dq, sq, bq)) != TR_OK) return rc;
+    const uint64_t dc[2] = {(uint64_t)kD, (uint64_t)B * Hkv * (cap > 0 ? cap : 1)};
+    const uint64_t sc[1] = {(uint64_t)kD * 2};
+    const uint32_t bc[2] = {64, c_rows};
+    if ((rc = tr_make_tmap_bf16(&tkc, Kc, 2, dc, sc, bc)) != TR_OK) return rc;
+    if ((rc = tr_make_tmap_bf16(&tvc, Vc, 2, dc, sc, bc)) != TR_OK) return rc;
+    const uint64_t dt[3] = {(uint64_t)kD, (uint64_t)Hkv, (uint64_t)B * N};
+    const uint64_t st[2] = {(uint64_t)kD * 2, (uint64_t)Hkv * kD * 2};
+    const uint32_t bt[3] = {64, 1, t_rows};
+    if ((rc = tr_make_tmap_bf16(&tkt, Kt, 3, dt, st, bt)) != TR_OK) return rc;
+    if ((rc = tr_make_tmap_bf16(&tvt, Vt, 3, dt, st, bt)) != TR_OK) return rc;
   }
   AttnArgs a;
-  a.Q = (const __nv_bfloat16 *)Q;
-  a.Kt = (const __nv_bfloat16 *)Kt;
-  a.Vt = (const __nv_bfloat16 *)Vt;
-  a.Kc = (const __nv_bfloat16 *)Kc;
-  a.Vc = (const __nv_bfloat16 *)Vc;
   a.L = L;
   a.O = O;
-  a.part_o = (float *)((char *)ws + w.o_off);
-  a.part_ml = (float2 *)((char *)ws + w.ml_off);
-  a.counters = (unsigned *)((char *)ws + w.cnt_off);
-  a.cap = cap;
+  a.part_o = (float *)((char *)ws + p.o_off);
+  a.part_ml = (float2 *)((char *)ws + p.ml_off);
+  a.status = tr_status_dev();
   a.B = B;
+  a.N = N;
   a.Hq = Hq;
   a.Hkv = Hkv;
-  a.CH = max_chunks(cap, N);
-  a.scale = scale;
-  a.status = tr_status_dev();
-  dim3 grid(a.CH, Hq, B);
-  attn_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(a, tree->dev);
+  a.G = p.G;
+  a.HG = p.HG;
+  a.cap = cap;
+  a.q_rows = (int)q_rows;
+  a.c_rows = (int)c_rows;
+  a.t_rows = (int)t_rows;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = (cudaStream_t)stream;
+  static bool attr_set[2][64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (p.MT == 1) {
+    if (dev >= 0 && dev < 64 && !attr_set[0][dev]) {
+      TR_TRY_CUDA(cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bytes<1>()));
+      attr_set[0][dev] = true;
+    }
+    attn_tc_kernel<1><<<p.grid, Cfg<1>::THREADS, smem_bytes<1>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
+  } else {
+    if (dev >= 0 && dev < 64 && !attr_set[1][dev]) {
+      TR_TRY_CUDA(cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_bytes<2>()));
+      attr_set[1][dev] = true;
+    }
+    attn_tc_kernel<2><<<p.grid, Cfg<2>::THREADS, smem_bytes<2>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
+  }
+  TR_LAUNCH_CHECK();
+  attn_merge_kernel<<<dim3(p.pairs, p.MT), 128, 0, s>>>(a, p.MT, p.grid);
   TR_LAUNCH_CHECK();
   return TR_OK;
 }

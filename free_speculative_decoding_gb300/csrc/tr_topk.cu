@@ -5,8 +5,8 @@
 // waves of short CTAs on 152 SMs whatever the row count.  Each thread keeps a
 // sorted register list of 64-bit keys (order-preserving value code in the
 // high word, complemented ID in the low word, so larger key = better and equal
-// values prefer the lower ID); a one-compare float threshold rejects almost
-// every element.  Lists merge by warp shuffles, then across warps, then across
+// values prefer the lower ID); a warp-wide floor computed from the lanes'
+// maxima rejects all but about 1% of the elements with one compare.  Lists merge by warp shuffles, then across warps, then across
 // the row's chunks in the last CTA to finish (an arrival counter in the
 // workspace, no spin-wait).
 #include "tr_internal.cuh"
@@ -15,9 +15,23 @@
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kUnroll = 4;
+constexpr int kWindow = 8192;       // elements a CTA holds in registers at once
 constexpr long long kChunk = 8192;  // target elements per CTA
 constexpr int kMaxSplits = 32;
+
+// K-th largest of the lanes' values (counting repeats), the same on every lane.
+__device__ __forceinline__ float warp_kth(float v, int K, int lane) {
+  float res = -INFINITY;
+  for (int r = 0; r < K; ++r) {
+    float m = v;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    res = m;
+    const unsigned who = __ballot_sync(0xffffffffu, v == m);
+    if (lane == __ffs(who) - 1) v = -INFINITY;
+  }
+  return res;
+}
 
 template <typename T>
 struct Elem;
@@ -32,6 +46,10 @@ struct Elem<float> {
     L.push(__uint_as_float(q.w), id + 3);
   }
   __device__ __forceinline__ static float load1(const float *p) { return __ldcs(p); }
+  __device__ __forceinline__ static uint4 nan_vec() { return make_uint4(0x7FC00000u, 0x7FC00000u, 0x7FC00000u, 0x7FC00000u); }
+  __device__ __forceinline__ static float vmax(const uint4 &q) {
+    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)), fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+  }
 };
 template <>
 struct Elem<__nv_bfloat16> {
@@ -46,6 +64,14 @@ struct Elem<__nv_bfloat16> {
     L.push(__uint_as_float(q.z & 0xFFFF0000u), id + 5);
     L.push(__uint_as_float(q.w << 16), id + 6);
     L.push(__uint_as_float(q.w & 0xFFFF0000u), id + 7);
+  }
+  __device__ __forceinline__ static uint4 nan_vec() { return make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u); }
+  __device__ __forceinline__ static float vmax(const uint4 &q) {
+    const float a = fmaxf(fmaxf(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u)),
+                          fmaxf(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u)));
+    const float b = fmaxf(fmaxf(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u)),
+                          fmaxf(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u)));
+    return fmaxf(a, b);
   }
   __device__ __forceinline__ static float load1(const __nv_bfloat16 *p) {
     const unsigned short u = __ldcs((const unsigned short *)p);
@@ -70,27 +96,32 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long lo
   L.init();
   long long done = lo;
   if (VEC) {
+    // The chunk is held in registers (one window of kWindow elements, more
+    // windows only for chunks longer than that).  A first pass takes each
+    // lane's maximum; the K-th largest lane maximum of the warp is reached by
+    // at least K elements of the warp, so anything strictly below it cannot be
+    // in the row's top K.  The second pass then pushes only the few elements
+    // at or above that floor into the lane's list.
     constexpr int kV = Elem<T>::kVec;
+    constexpr int NV = kWindow / (kThreads * kV);
     const uint4 *xv = reinterpret_cast<const uint4 *>(x + lo);
     const int nvec = (int)((hi - lo) / kV);
-    // warp-uniform trip count so the lanes can share their thresholds
-    for (int base = 0; base < nvec; base += kThreads * kUnroll) {
-      uint4 buf[kUnroll];
+    for (int base = 0; base < nvec; base += kThreads * NV) {  // warp-uniform trip count
+      uint4 buf[NV];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + tid + u * kThreads;
-        if (i < nvec) buf[u] = __ldcs(xv + i);
+      for (int u = 0; u < NV; ++u) {
+        const int i = base + u * kThreads + tid;
+        buf[u] = i < nvec ? __ldcs(xv + i) : Elem<T>::nan_vec();
       }
+      float lm = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int i = base + tid + u * kThreads;
+      for (int u = 0; u < NV; ++u) lm = fmaxf(lm, Elem<T>::vmax(buf[u]));
+      L.raise_floor(warp_kth(lm, K, lane));
+#pragma unroll
+      for (int u = 0; u < NV; ++u) {
+        const int i = base + u * kThreads + tid;
         if (i < nvec) Elem<T>::template push_vec<KMAX>(L, buf[u], (uint32_t)(lo + (long long)i * kV));
       }
-      // the best KMAX-th value of any lane bounds what can still enter the warp's top KMAX
-      float f = L.k[KMAX - 1] ? tr_key_val(L.k[KMAX - 1]) : -INFINITY;
-#pragma unroll
-      for (int off = 16; off; off >>= 1) f = fmaxf(f, __shfl_xor_sync(0xffffffffu, f, off));
-      L.raise_floor(f);
     }
     done = lo + (long long)nvec * kV;
   }
