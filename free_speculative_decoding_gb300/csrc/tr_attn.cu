@@ -51,6 +51,10 @@ constexpr int kMaxB = 1024;
 template <int MT>
 struct Cfg {
   static constexpr int STAGES = MT == 1 ? 3 : 2;
+  // MT == 1: two softmax warpgroups take alternate tiles, each with its own
+  // P buffer and O accumulator (combined at the end of a segment); MT == 2:
+  // one warpgroup per query head, one shared P buffer.
+  static constexpr int GROUPS = MT == 1 ? 2 : 1;
   static constexpr int PB = MT == 1 ? 2 : 1;      // P buffers (hi + lo parts each)
   static constexpr int Q_HALF = 128 * 128;        // 128 rows x 64 bf16 (one d-half), bytes
   static constexpr int KV_HALF = 64 * 128;        // 64 keys x 64 bf16
@@ -62,21 +66,23 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
   static constexpr int OFF_P = OFF_V + STAGES * KV_TILE;
   static constexpr int OFF_BAR = OFF_P + PB * MT * P_TILE;
-  static constexpr int THREADS = 64 + 128 * MT;
-  static constexpr int SOFT = 128 * MT;
-  static constexpr uint32_t TMEM_COLS = 256 * MT;
+  static constexpr int SOFT = 128 * MT * GROUPS;  // softmax threads
+  static constexpr int THREADS = 64 + SOFT;
+  static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t s_col(int buf, int m) { return (uint32_t)((buf * MT + m) * BN); }
-  __host__ __device__ static constexpr uint32_t o_col(int m) { return (uint32_t)(2 * MT * BN + m * kD); }
+  // accumulator o (0 .. MT*GROUPS-1) after the S buffers
+  __host__ __device__ static constexpr uint32_t o_col(int o) { return (uint32_t)(2 * MT * BN + o * kD); }
 };
 
 template <int S, int PB>
 struct Bars {
   uint64_t q_full, q_empty;
   uint64_t k_full[S], k_empty[S], v_full[S], v_empty[S];
-  uint64_t s_full[2], p_full[PB], pv_done[PB];
-  uint64_t o_full, o_empty, drain;
+  uint64_t s_full[2], s_empty[2], p_full[PB], pv_done[PB];
+  uint64_t o_full, o_empty, drain, ml_ready;
   uint32_t tmem;
   int abort;
+  float2 ml_x[2][128];  // second warpgroup's (m, l) per row, by segment parity
   int Ls[kMaxB];
   int pref[kMaxB + 1];  // first tile of sequence b in the global tile order
 };
@@ -154,14 +160,18 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&bars->s_full[b], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_empty[b], 128 * MT);
+    }
     for (int b = 0; b < PB; ++b) {
-      mbar_init(&bars->p_full[b], C::SOFT);
+      mbar_init(&bars->p_full[b], 128 * MT);
       mbar_init(&bars->pv_done[b], 1);
     }
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, C::SOFT);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->ml_ready, 128);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -280,63 +290,73 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           break;
         }
         tc_fence_after();
-        for (int u = 0; u <= T && ok; ++u) {
-          if (u < T) {
-            const int s = kc % S;
-            if (!mbar_wait(&bars->k_full[s], (kc / S) & 1, abort)) {
-              give_up();
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const int sb = (gt + u) & 1;
-            const uint32_t kb = smem_u32(smem + C::OFF_K + s * C::KV_TILE);
-            for (int m = 0; m < MT; ++m) {
-              const uint32_t qb = smem_u32(smem + C::OFF_Q + m * 2 * C::Q_HALF);
+        // S = Q.K^T of tile u of the segment, once its S buffer has been read
+        // by the softmax of the tile two before it
+        auto issue_qk = [&](int u) -> bool {
+          const int gq = gt + u, sb = gq & 1;
+          if (gq >= 2 && !mbar_wait(&bars->s_empty[sb], ((gq - 2) >> 1) & 1, abort)) return false;
+          const int s = kc % S;
+          if (!mbar_wait(&bars->k_full[s], (kc / S) & 1, abort)) return false;
+          tc_fence_after();
+          const uint32_t kb = smem_u32(smem + C::OFF_K + s * C::KV_TILE);
+          for (int m = 0; m < MT; ++m) {
+            const uint32_t qb = smem_u32(smem + C::OFF_Q + m * 2 * C::Q_HALF);
 #pragma unroll
-              for (int ks = 0; ks < kD / 16; ++ks)
-                mma_bf16(tmem + C::s_col(sb, m), desc_kmajor_sw128(qb + (ks >> 2) * C::Q_HALF + (ks & 3) * 32),
-                         desc_kmajor_sw128(kb + (ks >> 2) * C::KV_HALF + (ks & 3) * 32), kIdescQK, ks > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars->k_empty[s]);
-            mma_commit(&bars->s_full[sb]);
-            if (u == T - 1) mma_commit(&bars->q_empty);
-            ++kc;
+            for (int ks = 0; ks < kD / 16; ++ks)
+              mma_bf16(tmem + C::s_col(sb, m), desc_kmajor_sw128(qb + (ks >> 2) * C::Q_HALF + (ks & 3) * 32),
+                       desc_kmajor_sw128(kb + (ks >> 2) * C::KV_HALF + (ks & 3) * 32), kIdescQK, ks > 0 ? 1u : 0u);
           }
-          if (u >= 1) {
-            const int j = u - 1, gj = gt + j, pb = gj % PB;
-            if (!mbar_wait(&bars->p_full[pb], (gj / PB) & 1, abort)) {
-              give_up();
-              ok = false;
-              break;
-            }
-            const int s = vc % S;
-            if (!mbar_wait(&bars->v_full[s], (vc / S) & 1, abort)) {
-              give_up();
-              ok = false;
-              break;
-            }
-            if (j == 0 && !mbar_wait(&bars->o_empty, (sc & 1) ^ 1, abort)) {
-              give_up();
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t vb = smem_u32(smem + C::OFF_V + s * C::KV_TILE);
-            for (int m = 0; m < MT; ++m) {
-              const uint32_t pbase = smem_u32(smem + C::OFF_P + (pb * MT + m) * C::P_TILE);
-#pragma unroll
-              for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int ks = 0; ks < BN / 16; ++ks)
-                  mma_bf16(tmem + C::o_col(m), desc_kmajor_sw128(pbase + part * C::P_PART + ks * 32),
-                           desc_mnmajor_sw128(vb + ks * 2048, C::KV_HALF), kIdescPV,
-                           (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-            }
-            mma_commit(&bars->v_empty[s]);
-            mma_commit(&bars->pv_done[pb]);
-            ++vc;
+          mma_commit(&bars->k_empty[s]);
+          mma_commit(&bars->s_full[sb]);
+          if (u == T - 1) mma_commit(&bars->q_empty);
+          ++kc;
+          return true;
+        };
+        for (int u = 0; u < T && u < 2 && ok; ++u)
+          if (!issue_qk(u)) {
+            give_up();
+            ok = false;
           }
+        for (int j = 0; j < T && ok; ++j) {
+          if (j + 2 < T && !issue_qk(j + 2)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          // O += P.V of tile j
+          const int gj = gt + j, pb = gj % PB;
+          if (!mbar_wait(&bars->p_full[pb], (gj / PB) & 1, abort)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          const int s = vc % S;
+          if (!mbar_wait(&bars->v_full[s], (vc / S) & 1, abort)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          if (j == 0 && !mbar_wait(&bars->o_empty, (sc & 1) ^ 1, abort)) {
+            give_up();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t vb = smem_u32(smem + C::OFF_V + s * C::KV_TILE);
+          for (int m = 0; m < MT; ++m) {
+            const uint32_t pbase = smem_u32(smem + C::OFF_P + (pb * MT + m) * C::P_TILE);
+            const int o = MT == 1 ? (gj & 1) : m;  // MT == 1: the tile's warpgroup owns accumulator gj & 1
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int ks = 0; ks < BN / 16; ++ks)
+                mma_bf16(tmem + C::o_col(o), desc_kmajor_sw128(pbase + part * C::P_PART + ks * 32),
+                         desc_mnmajor_sw128(vb + ks * 2048, C::KV_HALF), kIdescPV,
+                         (j >= C::GROUPS || part > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->v_empty[s]);
+          mma_commit(&bars->pv_done[pb]);
+          ++vc;
         }
         if (!ok) break;
         mma_commit(&bars->o_full);
@@ -347,8 +367,11 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax
-    const int mt = (warp - 2) >> 2;
-    const int quad = warp & 3;  // TMEM lanes quad*32 .. +31
+    const int su = (warp - 2) >> 2;            // softmax unit: warpgroup (MT == 1) or query head (MT == 2)
+    const int grp = MT == 1 ? su : 0;
+    const int mt = MT == 1 ? 0 : su;
+    const int oacc = su;                       // this unit's O accumulator
+    const int quad = warp & 3;                 // TMEM lanes quad*32 .. +31
     const int r = quad * 32 + lane;
     const bool warp_active = quad * 32 < N;
     const bool row_valid = r < N;
@@ -372,13 +395,16 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       const int T = sg.n;
       const int h = sg.g * a.G + sg.hg * MT + mt;
       float m_run = -INFINITY, l_run = 0.f;
+      int done_here = 0;  // tiles of this segment this unit has folded into its accumulator
       for (int u = 0; u < T && ok; ++u) {
         const int gtt = gt + u, sb = gtt & 1, pb = gtt % PB;
+        if (MT == 1 && (gtt & 1) != grp) continue;  // the other warpgroup's tile
         if (!wwait(&bars->s_full[sb], (gtt >> 1) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        if (!warp_active) mbar_arrive(&bars->s_empty[sb]);
         if (warp_active) {
           float sv[BN];
           {
@@ -390,30 +416,42 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) sv[32 + c] = tmp[c];
           }
+          // S is in registers: the MMA may overwrite this buffer with the next tile's scores
+          tc_fence_before();
+          mbar_arrive(&bars->s_empty[sb]);
           const int j = sg.j0 + u;
           const bool cache = j < sg.n_ct;
           const int key0 = j * BN;
-          const int node0 = (j - sg.n_ct) * BN;
           float mx = -INFINITY;
+          if (cache && key0 + BN <= sg.Lb) {
+            // a full cache tile: every key is visible (rows past N are never stored)
 #pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            bool valid;
-            if (cache) {
-              valid = key0 + c < sg.Lb;
-            } else {
-              const int nd = node0 + c;
-              const unsigned long long w = nd < 64 ? anc0 : anc1;
-              valid = nd < N && ((w >> (nd & 63)) & 1ull);
+            for (int c = 0; c < BN; ++c) {
+              sv[c] *= a.scale_log2;
+              mx = fmaxf(mx, sv[c]);
             }
-            valid = valid && row_valid;
-            sv[c] = valid ? sv[c] * a.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, sv[c]);
+          } else {
+            const int node0 = (j - sg.n_ct) * BN;
+#pragma unroll
+            for (int c = 0; c < BN; ++c) {
+              bool valid;
+              if (cache) {
+                valid = key0 + c < sg.Lb;
+              } else {
+                const int nd = node0 + c;
+                const unsigned long long w = nd < 64 ? anc0 : anc1;
+                valid = nd < N && ((w >> (nd & 63)) & 1ull);
+              }
+              valid = valid && row_valid;
+              sv[c] = valid ? sv[c] * a.scale_log2 : -INFINITY;
+              mx = fmaxf(mx, sv[c]);
+            }
           }
           const float m_new = fmaxf(m_run, mx);
           const bool need = m_new > m_run + kRescaleLog2;  // also true for the row's first finite maximum
-          if (__any_sync(0xffffffffu, need && u > 0)) {
-            // O already holds earlier tiles: wait for the last PV, then scale O in TMEM
-            const int gp = gtt - 1;
+          if (__any_sync(0xffffffffu, need && done_here > 0)) {
+            // O already holds this unit's earlier tiles: wait for the last PV into it, then scale it
+            const int gp = gtt - PB;
             if (!wwait(&bars->pv_done[gp % PB], (gp / PB) & 1)) {
               ok = false;
               break;
@@ -423,10 +461,10 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
 #pragma unroll 1
             for (int c0 = 0; c0 < kD; c0 += 32) {
               float ov[32];
-              tmem_ld32(tmem + lane_off + C::o_col(mt) + c0, ov);
+              tmem_ld32(tmem + lane_off + C::o_col(oacc) + c0, ov);
 #pragma unroll
               for (int c = 0; c < 32; ++c) ov[c] *= f;
-              tmem_st32(tmem + lane_off + C::o_col(mt) + c0, ov);
+              tmem_st32(tmem + lane_off + C::o_col(oacc) + c0, ov);
             }
           }
           if (need) {
@@ -439,14 +477,16 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
             break;
           }
           uint8_t *prow = prow_base + pb * MT * C::P_TILE;
+          // ex2(-inf) = 0 for masked keys; a row that has seen no visible key yet
+          // (m_run = -inf, all its keys masked) subtracts 0 instead of -inf
+          const float m_sub = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
           for (int c8 = 0; c8 < BN / 8; ++c8) {
             uint32_t whi[4], wlo[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float x0 = sv[c8 * 8 + 2 * q], x1 = sv[c8 * 8 + 2 * q + 1];
-              const float p0 = x0 == -INFINITY ? 0.f : ex2(x0 - m_run);
-              const float p1 = x1 == -INFINITY ? 0.f : ex2(x1 - m_run);
+              const float p0 = ex2(sv[c8 * 8 + 2 * q] - m_sub);
+              const float p1 = ex2(sv[c8 * 8 + 2 * q + 1] - m_sub);
               l_run += p0 + p1;
               const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
               const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(hi), p1 - __high2float(hi));
@@ -459,6 +499,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           }
           fence_proxy_async_smem();
         }
+        ++done_here;
         tc_fence_before();
         mbar_arrive(&bars->p_full[pb]);
       }
@@ -466,26 +507,49 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       // ---- end of the segment: normalised output or a partial
       if (!wwait(&bars->o_full, sc & 1)) break;
       tc_fence_after();
-      if (warp_active) {
-        const int slot = blockIdx.x * 2 + (sg.first_of_cta ? 0 : 1);
-        const long long prow_idx = ((long long)slot * MT + mt) * N + r;
-        const float inv = row_valid && l_run > 0.f ? 1.f / l_run : 0.f;
-        float *dst = sg.complete ? a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD : a.part_o + prow_idx * kD;
+      if (MT == 1 && grp == 1) {
+        // hand this warpgroup's (m, l) to the first warpgroup, which combines the two accumulators
+        bars->ml_x[sc & 1][r] = make_float2(done_here ? m_run : -INFINITY, done_here ? l_run : 0.f);
+        mbar_arrive(&bars->ml_ready);
+      } else {
+        float2 other = make_float2(-INFINITY, 0.f);
+        if (MT == 1) {
+          if (!wwait(&bars->ml_ready, sc & 1)) break;
+          other = bars->ml_x[sc & 1][r];
+        }
+        if (!done_here) {
+          m_run = -INFINITY;
+          l_run = 0.f;
+        }
+        const float M = fmaxf(m_run, other.x);
+        const float wa = m_run == -INFINITY ? 0.f : ex2(m_run - M);
+        const float wb = other.x == -INFINITY ? 0.f : ex2(other.x - M);
+        const float l = l_run * wa + other.y * wb;
+        if (warp_active) {
+          const int slot = blockIdx.x * 2 + (sg.first_of_cta ? 0 : 1);
+          const long long prow_idx = ((long long)slot * MT + mt) * N + r;
+          const float scale_out = sg.complete ? (row_valid && l > 0.f ? 1.f / l : 0.f) : 1.f;
+          const bool use_a = wa != 0.f, use_b = MT == 1 && wb != 0.f;
+          float *dst = sg.complete ? a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD : a.part_o + prow_idx * kD;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-          float ov[32];
-          tmem_ld32(tmem + lane_off + C::o_col(mt) + c0, ov);
-          if (row_valid) {
+          for (int c0 = 0; c0 < kD; c0 += 32) {
+            float oa[32], ob[32];
+            tmem_ld32(tmem + lane_off + C::o_col(oacc) + c0, oa);
+            if (MT == 1) tmem_ld32(tmem + lane_off + C::o_col(1) + c0, ob);
+            if (row_valid) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 4) {
-              const float4 v4 = sg.complete
-                                    ? make_float4(ov[c] * inv, ov[c + 1] * inv, ov[c + 2] * inv, ov[c + 3] * inv)
-                                    : make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
-              *reinterpret_cast<float4 *>(dst + c0 + c) = v4;
+              for (int c = 0; c < 32; ++c) {
+                float v = use_a ? oa[c] * wa : 0.f;
+                if (use_b) v += ob[c] * wb;
+                oa[c] = v * scale_out;
+              }
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4 *>(dst + c0 + c) = make_float4(oa[c], oa[c + 1], oa[c + 2], oa[c + 3]);
             }
           }
+          if (!sg.complete && row_valid) a.part_ml[prow_idx] = make_float2(M, l);
         }
-        if (!sg.complete && row_valid) a.part_ml[prow_idx] = make_float2(m_run, l_run);
       }
       tc_fence_before();
       mbar_arrive(&bars->o_empty);

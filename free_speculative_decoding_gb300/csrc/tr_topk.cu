@@ -46,7 +46,14 @@ struct Elem<float> {
     L.push(__uint_as_float(q.w), id + 3);
   }
   __device__ __forceinline__ static float load1(const float *p) { return __ldcs(p); }
+  __device__ __forceinline__ static float load_again(const float *p) { return __ldcg(p); }
   __device__ __forceinline__ static uint4 nan_vec() { return make_uint4(0x7FC00000u, 0x7FC00000u, 0x7FC00000u, 0x7FC00000u); }
+  __device__ __forceinline__ static void unpack(const uint4 &q, float (&e)[4]) {
+    e[0] = __uint_as_float(q.x);
+    e[1] = __uint_as_float(q.y);
+    e[2] = __uint_as_float(q.z);
+    e[3] = __uint_as_float(q.w);
+  }
   __device__ __forceinline__ static float vmax(const uint4 &q) {
     return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)), fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
   }
@@ -66,12 +73,25 @@ struct Elem<__nv_bfloat16> {
     L.push(__uint_as_float(q.w & 0xFFFF0000u), id + 7);
   }
   __device__ __forceinline__ static uint4 nan_vec() { return make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u); }
+  __device__ __forceinline__ static void unpack(const uint4 &q, float (&e)[8]) {
+    e[0] = __uint_as_float(q.x << 16);
+    e[1] = __uint_as_float(q.x & 0xFFFF0000u);
+    e[2] = __uint_as_float(q.y << 16);
+    e[3] = __uint_as_float(q.y & 0xFFFF0000u);
+    e[4] = __uint_as_float(q.z << 16);
+    e[5] = __uint_as_float(q.z & 0xFFFF0000u);
+    e[6] = __uint_as_float(q.w << 16);
+    e[7] = __uint_as_float(q.w & 0xFFFF0000u);
+  }
   __device__ __forceinline__ static float vmax(const uint4 &q) {
     const float a = fmaxf(fmaxf(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u)),
                           fmaxf(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u)));
     const float b = fmaxf(fmaxf(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u)),
                           fmaxf(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u)));
     return fmaxf(a, b);
+  }
+  __device__ __forceinline__ static float load_again(const __nv_bfloat16 *p) {
+    return __uint_as_float((uint32_t)__ldcg((const unsigned short *)p) << 16);
   }
   __device__ __forceinline__ static float load1(const __nv_bfloat16 *p) {
     const unsigned short u = __ldcs((const unsigned short *)p);
@@ -100,28 +120,52 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long lo
     // windows only for chunks longer than that).  A first pass takes each
     // lane's maximum; the K-th largest lane maximum of the warp is reached by
     // at least K elements of the warp, so anything strictly below it cannot be
-    // in the row's top K.  The second pass then pushes only the few elements
-    // at or above that floor into the lane's list.
+    // in the row's top K.  The second pass compacts the few elements at or
+    // above that floor into the warp's shared-memory slots with one ballot per
+    // element position, and a single, non-unrolled loop inserts them into the
+    // lane lists (keeping the unrolled part small enough for the instruction
+    // cache).
     constexpr int kV = Elem<T>::kVec;
     constexpr int NV = kWindow / (kThreads * kV);
+    constexpr int kSlots = kWindow / (kThreads / 32);  // a warp's whole share of a window
+    __shared__ unsigned short cand_o[kThreads / 32][kSlots];  // offsets in the window
     const uint4 *xv = reinterpret_cast<const uint4 *>(x + lo);
     const int nvec = (int)((hi - lo) / kV);
+    const unsigned lt_mask = (1u << lane) - 1u;
     for (int base = 0; base < nvec; base += kThreads * NV) {  // warp-uniform trip count
       uint4 buf[NV];
 #pragma unroll
       for (int u = 0; u < NV; ++u) {
         const int i = base + u * kThreads + tid;
-        buf[u] = i < nvec ? __ldcs(xv + i) : Elem<T>::nan_vec();
+        buf[u] = i < nvec ? __ldcs(xv + i) : Elem<T>::nan_vec();  // NaN never passes a compare
       }
       float lm = -INFINITY;
 #pragma unroll
       for (int u = 0; u < NV; ++u) lm = fmaxf(lm, Elem<T>::vmax(buf[u]));
       L.raise_floor(warp_kth(lm, K, lane));
+      const float thr = L.thr;
+      int nc = 0;  // warp-uniform
 #pragma unroll
       for (int u = 0; u < NV; ++u) {
-        const int i = base + u * kThreads + tid;
-        if (i < nvec) Elem<T>::template push_vec<KMAX>(L, buf[u], (uint32_t)(lo + (long long)i * kV));
+        float e[kV];
+        Elem<T>::unpack(buf[u], e);
+#pragma unroll
+        for (int q = 0; q < kV; ++q) {
+          const bool c = e[q] >= thr;
+          const unsigned bal = __ballot_sync(0xffffffffu, c);
+          if (c) cand_o[warp][nc + __popc(bal & lt_mask)] = (unsigned short)((u * kThreads + tid) * kV + q);
+          nc += __popc(bal);
+        }
       }
+      __syncwarp();
+      const long long id0 = lo + (long long)base * kV;
+      // the few candidates' values are read again (from L2, just streamed through)
+#pragma unroll 1
+      for (int k = lane; k < nc; k += 32) {
+        const long long id = id0 + cand_o[warp][k];
+        L.push(Elem<T>::load_again(x + id), (uint32_t)id);
+      }
+      __syncwarp();
     }
     done = lo + (long long)nvec * kV;
   }
