@@ -422,13 +422,13 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           const int j = sg.j0 + u;
           const bool cache = j < sg.n_ct;
           const int key0 = j * BN;
-          float mx = -INFINITY;
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
           if (cache && key0 + BN <= sg.Lb) {
             // a full cache tile: every key is visible (rows past N are never stored)
 #pragma unroll
             for (int c = 0; c < BN; ++c) {
               sv[c] *= a.scale_log2;
-              mx = fmaxf(mx, sv[c]);
+              mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
             }
           } else {
             const int node0 = (j - sg.n_ct) * BN;
@@ -444,9 +444,10 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
               }
               valid = valid && row_valid;
               sv[c] = valid ? sv[c] * a.scale_log2 : -INFINITY;
-              mx = fmaxf(mx, sv[c]);
+              mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
             }
           }
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
           const float m_new = fmaxf(m_run, mx);
           const bool need = m_new > m_run + kRescaleLog2;  // also true for the row's first finite maximum
           if (__any_sync(0xffffffffu, need && done_here > 0)) {
@@ -480,6 +481,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           // ex2(-inf) = 0 for masked keys; a row that has seen no visible key yet
           // (m_run = -inf, all its keys masked) subtracts 0 instead of -inf
           const float m_sub = m_run == -INFINITY ? 0.f : m_run;
+          float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
 #pragma unroll
           for (int c8 = 0; c8 < BN / 8; ++c8) {
             uint32_t whi[4], wlo[4];
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
             for (int q = 0; q < 4; ++q) {
               const float p0 = ex2(sv[c8 * 8 + 2 * q] - m_sub);
               const float p1 = ex2(sv[c8 * 8 + 2 * q + 1] - m_sub);
-              l_run += p0 + p1;
+              l4[q] += p0 + p1;
               const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
               const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(hi), p1 - __high2float(hi));
               whi[q] = *reinterpret_cast<const uint32_t *>(&hi);
@@ -497,6 +499,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
             *reinterpret_cast<uint4 *>(prow + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
             *reinterpret_cast<uint4 *>(prow + C::P_PART + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
           }
+          l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
           fence_proxy_async_smem();
         }
         ++done_here;

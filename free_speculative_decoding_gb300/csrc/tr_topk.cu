@@ -14,9 +14,10 @@
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kWindow = 8192;       // elements a CTA holds in registers at once
-constexpr long long kChunk = 8192;  // target elements per CTA
+constexpr int kThreads = 256;
+constexpr int kWindow = 16384;            // elements a CTA holds in registers (its whole chunk)
+constexpr long long kChunk = kWindow;     // target elements per CTA
+constexpr int kRankKeys = 1024;           // keys ranked directly (also all chunks' lists of a row)
 constexpr int kMaxSplits = 32;
 
 // K-th largest of the lanes' values (counting repeats), the same on every lane.
@@ -99,114 +100,156 @@ struct Elem<__nv_bfloat16> {
   }
 };
 
+// The K largest of n distinct keys in shared memory, sorted, into out[0..K)
+// (0 where fewer than K): each key's rank is the number of larger keys.
+__device__ __forceinline__ void rank_select(const unsigned long long *keys, int n, int K, unsigned long long *out) {
+  for (int k = threadIdx.x; k < K; k += blockDim.x) out[k] = 0ull;
+  __syncthreads();
+  for (int k = threadIdx.x; k < n; k += blockDim.x) {
+    const unsigned long long key = keys[k];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += keys[j] > key;
+    if (rank < K && key) out[rank] = key;
+  }
+  __syncthreads();
+}
+
 template <typename T, int KMAX, bool VEC>
 __global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long long V, long long ld, int K,
                                                         long long chunk, int32_t *ids, float *vals,
                                                         unsigned long long *part, unsigned *counters) {
+  __shared__ unsigned short cand_o[kWindow];          // candidate offsets within the chunk
+  __shared__ unsigned long long keys[kRankKeys];       // keys being ranked
+  __shared__ unsigned long long top[TR_MAX_K];
   __shared__ unsigned long long warp_keys[kThreads / 32][KMAX];
-  __shared__ int is_last;
+  __shared__ float wfloor[kThreads / 32];
+  __shared__ int count, is_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, splits = gridDim.x;
   const long long row = blockIdx.y;
   const T *x = logits + row * ld;
   const long long lo = split * chunk;
   const long long hi = min(V, lo + chunk);
+  if (tid == 0) count = 0;
 
-  TopList<KMAX> L;
-  L.init();
-  long long done = lo;
+  bool ranked = false;
   if (VEC) {
-    // The chunk is held in registers (one window of kWindow elements, more
-    // windows only for chunks longer than that).  A first pass takes each
-    // lane's maximum; the K-th largest lane maximum of the warp is reached by
-    // at least K elements of the warp, so anything strictly below it cannot be
-    // in the row's top K.  The second pass compacts the few elements at or
-    // above that floor into the warp's shared-memory slots with one ballot per
-    // element position, and a single, non-unrolled loop inserts them into the
-    // lane lists (keeping the unrolled part small enough for the instruction
-    // cache).
+    // The chunk sits in registers.  The K-th largest lane maximum of a warp is
+    // reached by at least K elements of that warp, so no element strictly
+    // below the largest such warp floor can be in the row's top K.  Elements
+    // at or above it (about 1% of random logits) are compacted into shared
+    // memory with one ballot per element position and ranked directly.
     constexpr int kV = Elem<T>::kVec;
     constexpr int NV = kWindow / (kThreads * kV);
-    constexpr int kSlots = kWindow / (kThreads / 32);  // a warp's whole share of a window
-    __shared__ unsigned short cand_o[kThreads / 32][kSlots];  // offsets in the window
     const uint4 *xv = reinterpret_cast<const uint4 *>(x + lo);
     const int nvec = (int)((hi - lo) / kV);
+    uint4 buf[NV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      const int i = u * kThreads + tid;
+      buf[u] = i < nvec ? __ldcs(xv + i) : Elem<T>::nan_vec();  // NaN never passes a compare
+    }
+    float lm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < NV; ++u) lm = fmaxf(lm, Elem<T>::vmax(buf[u]));
+    const float wk = warp_kth(lm, K, lane);
+    if (lane == 0) wfloor[warp] = wk;
+    __syncthreads();
+    float floor_v = wfloor[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) floor_v = fmaxf(floor_v, wfloor[w]);
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = 0; base < nvec; base += kThreads * NV) {  // warp-uniform trip count
-      uint4 buf[NV];
 #pragma unroll
-      for (int u = 0; u < NV; ++u) {
-        const int i = base + u * kThreads + tid;
-        buf[u] = i < nvec ? __ldcs(xv + i) : Elem<T>::nan_vec();  // NaN never passes a compare
-      }
-      float lm = -INFINITY;
+    for (int u = 0; u < NV; ++u) {
+      float e[kV];
+      Elem<T>::unpack(buf[u], e);
 #pragma unroll
-      for (int u = 0; u < NV; ++u) lm = fmaxf(lm, Elem<T>::vmax(buf[u]));
-      L.raise_floor(warp_kth(lm, K, lane));
-      const float thr = L.thr;
-      int nc = 0;  // warp-uniform
-#pragma unroll
-      for (int u = 0; u < NV; ++u) {
-        float e[kV];
-        Elem<T>::unpack(buf[u], e);
-#pragma unroll
-        for (int q = 0; q < kV; ++q) {
-          const bool c = e[q] >= thr;
-          const unsigned bal = __ballot_sync(0xffffffffu, c);
-          if (c) cand_o[warp][nc + __popc(bal & lt_mask)] = (unsigned short)((u * kThreads + tid) * kV + q);
-          nc += __popc(bal);
+      for (int q = 0; q < kV; ++q) {
+        const bool c = e[q] >= floor_v;
+        const unsigned bal = __ballot_sync(0xffffffffu, c);
+        if (bal) {
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&count, __popc(bal));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          if (c) cand_o[base + __popc(bal & lt_mask)] = (unsigned short)((u * kThreads + tid) * kV + q);
         }
       }
-      __syncwarp();
-      const long long id0 = lo + (long long)base * kV;
-      // the few candidates' values are read again (from L2, just streamed through)
-#pragma unroll 1
-      for (int k = lane; k < nc; k += 32) {
-        const long long id = id0 + cand_o[warp][k];
+    }
+    // the ragged end of the chunk (fewer than one vector)
+    const long long tail0 = lo + (long long)nvec * kV;
+    if (tail0 + tid < hi) {
+      const float v = Elem<T>::load1(x + tail0 + tid);
+      if (v >= floor_v) cand_o[atomicAdd(&count, 1)] = (unsigned short)(tail0 + tid - lo);
+    }
+    __syncthreads();
+    const int n = count;
+    if (n <= kRankKeys) {
+      for (int k = tid; k < n; k += kThreads) {
+        const long long id = lo + cand_o[k];
+        keys[k] = tr_key(tr_ord(Elem<T>::load_again(x + id)), (uint32_t)id);
+      }
+      rank_select(keys, n, K, top);
+      ranked = true;
+    } else {
+      // many ties at the floor: fold the candidates through register lists
+      TopList<KMAX> L;
+      L.init();
+      for (int k = tid; k < n; k += kThreads) {
+        const long long id = lo + cand_o[k];
         L.push(Elem<T>::load_again(x + id), (uint32_t)id);
       }
-      __syncwarp();
-    }
-    done = lo + (long long)nvec * kV;
-  }
-  for (long long i = done + tid; i < hi; i += kThreads) L.push(Elem<T>::load1(x + i), (uint32_t)i);
-
-  // block merge
-  unsigned long long mine = warp_merge<KMAX>(L, lane);
-  if (lane < KMAX) warp_keys[warp][lane] = mine;
-  __syncthreads();
-  if (warp != 0) return;
-  L.init();
-  if (lane < kThreads / 32) {
+      unsigned long long mine = warp_merge<KMAX>(L, lane);
+      if (lane < KMAX) warp_keys[warp][lane] = mine;
+      __syncthreads();
+      if (warp == 0) {
+        L.init();
+        if (lane < kThreads / 32)
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) L.k[j] = warp_keys[lane][j];
+          for (int j = 0; j < KMAX; ++j) L.k[j] = warp_keys[lane][j];
+        mine = warp_merge<KMAX>(L, lane);
+        if (lane < K) top[lane] = mine;
+      }
+      __syncthreads();
+      ranked = true;
+    }
   }
-  mine = warp_merge<KMAX>(L, lane);
+  if (!ranked) {
+    // rows that are not 16-byte aligned: a plain scan through register lists
+    TopList<KMAX> L;
+    L.init();
+    for (long long i = lo + tid; i < hi; i += kThreads) L.push(Elem<T>::load1(x + i), (uint32_t)i);
+    unsigned long long mine = warp_merge<KMAX>(L, lane);
+    if (lane < KMAX) warp_keys[warp][lane] = mine;
+    __syncthreads();
+    if (warp == 0) {
+      L.init();
+      if (lane < kThreads / 32)
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) L.k[j] = warp_keys[lane][j];
+      mine = warp_merge<KMAX>(L, lane);
+      if (lane < K) top[lane] = mine;
+    }
+    __syncthreads();
+  }
 
   if (splits > 1) {
-    // publish this chunk's list; the row's last CTA to arrive merges them all
-    if (lane < KMAX) part[(row * splits + split) * KMAX + lane] = mine;
+    // publish this chunk's top K; the row's last CTA to arrive ranks all chunks' keys
+    if (tid < K) part[(row * splits + split) * KMAX + tid] = top[tid];
     __threadfence();
-    __syncwarp();
-    if (lane == 0) is_last = atomicAdd(&counters[row], 1u) == (unsigned)(splits - 1);
-    __syncwarp();
+    __syncthreads();
+    if (tid == 0) is_last = atomicAdd(&counters[row], 1u) == (unsigned)(splits - 1);
+    __syncthreads();
     if (!is_last) return;
     __threadfence();
-    L.init();
-    for (int sp = lane; sp < splits; sp += 32) {
-      const unsigned long long *src = part + (row * splits + sp) * KMAX;
-      for (int j = 0; j < KMAX; ++j) {
-        const unsigned long long key = __ldcg(src + j);
-        if (key == 0ull) break;
-        list_insert<KMAX>(L.k, key);
-      }
-    }
-    mine = warp_merge<KMAX>(L, lane);
-    if (lane == 0) counters[row] = 0u;
+    const int n = splits * K;
+    for (int k = tid; k < n; k += kThreads) keys[k] = __ldcg(part + (row * splits + k / K) * KMAX + k % K);
+    rank_select(keys, n, K, top);
+    if (tid == 0) counters[row] = 0u;
   }
-  if (lane < K) {
-    ids[row * K + lane] = mine ? (int32_t)tr_key_id(mine) : -1;
-    if (vals) vals[row * K + lane] = mine ? tr_key_val(mine) : -INFINITY;
+  if (tid < K) {
+    const unsigned long long key = top[tid];
+    ids[row * K + tid] = key ? (int32_t)tr_key_id(key) : -1;
+    if (vals) vals[row * K + tid] = key ? tr_key_val(key) : -INFINITY;
   }
 }
 
@@ -255,7 +298,7 @@ int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, 
   const int splits = tr_topk_plan_splits(rows, V);
   const long long chunk = splits > 1 ? plan_chunk(V, splits) : V;
   const size_t esz = ftype == TR_F32 ? 4 : 2;
-  const bool vec = ((uintptr_t)logits % 16 == 0) && ((ld * (int64_t)esz) % 16 == 0);
+  const bool vec = ((uintptr_t)logits % 16 == 0) && ((ld * (int64_t)esz) % 16 == 0) && chunk <= kWindow;
   const size_t pb = part_bytes_for(rows, splits, K);
   const int km = tr_kmax(K);
 #define TR_TOPK_CASE(T, KM) launch<T, KM>(logits, rows, V, ld, K, splits, chunk, vec, ids, vals, ws, pb, s)
