@@ -15,28 +15,37 @@
 // kernel merges them.
 //
 // Per CTA:
-//   warp 0      TMA producer: the pair's Q tile(s) (3-D map over [B*N, Hq, d]),
-//               then K and V tiles of 64 keys from the cache (2-D map over
-//               [B*Hkv*cap, d]) or the tree (3-D map over [B*N, Hkv, d]), all
-//               with the 128-byte swizzle, into separate K and V rings;
-//   warp 1      one thread issues tcgen05.mma: S = Q.K^T (M128 x N64 x K128,
-//               fp32 in TMEM, double-buffered) and O += P.V (M128 x N128 x K64,
-//               V read as an MN-major operand, O in TMEM across the segment);
-//   warps 2..   softmax, one query row per thread (one TMEM lane): the mask
+//   warp 0      TMA producer of Q (3-D map over [B*N, Hq, d]) and of the K
+//               ring: tiles of 64 keys from the cache (2-D map over
+//               [B*Hkv*cap, d]) or the tree (3-D map over [B*N, Hkv, d]);
+//   warp 2      TMA producer of the V ring, same maps for V; the two rings
+//               run independently, so a V stage still held by a PV product
+//               never stops the K stream;
+//   warp 1      one thread issues tcgen05.mma as the operands become ready
+//               (non-blocking polls, so neither stream waits behind the
+//               other): S = Q.K^T (M128 x N64 x K128, fp32 in TMEM) and
+//               O += P.V (M128 x N128 x K64) with P read from TMEM and V
+//               from shared memory as an MN-major operand;
+//   warps 3..   softmax, one query row per thread (one TMEM lane): the mask
 //               (key < L for the cache, ancestor bit for the tree), exp2 with a
 //               running maximum that only rescales O when it grows by more
-//               than 2^8, P written to shared memory in the swizzled K-major
-//               layout the next MMA reads.  P goes in two bf16 parts, hi =
-//               bf16(p) and lo = bf16(p - hi), both multiplied with V, so the
-//               weights reach the accumulator with ~2^-17 relative error
-//               instead of bf16's 2^-9.  At the end of a segment the same
-//               threads normalise O or write the partial.
-// MT query heads sharing one KV head are processed together (MT = 2 for
-// grouped-query attention), so every K/V tile feeds 128*MT query rows.
+//               than 2^8, and P written back over the S columns it came from.
+//               P goes in two bf16 parts, hi = bf16(p) and lo = bf16(p - hi),
+//               both multiplied with V, so the weights reach the accumulator
+//               with ~2^-17 relative error instead of bf16's 2^-9.  At the end
+//               of a segment the same threads normalise O or write the
+//               partial.
+// TMEM holds two O accumulators (128 columns each) and four S/P buffers of
+// 64 columns; a buffer is reused by the QK product four tiles later, once the
+// PV product that read its P has completed.  With MT = 1 two softmax
+// warpgroups take alternate tiles into their own accumulators (combined at
+// the end of a segment); with MT = 2 the two query heads sharing one KV head
+// are processed together (grouped-query attention), one warpgroup and one
+// accumulator per head, so every K/V tile feeds 256 query rows.
 //
-// Every mbarrier wait is bounded in time; a wait that gives up sets
-// TR_DEV_TIMEOUT and raises a block-wide abort flag; the roles drain their
-// in-flight copies and MMAs, TMEM is freed and the kernel returns.
+// Every wait is bounded in time; a wait that gives up sets TR_DEV_TIMEOUT and
+// raises a block-wide abort flag; the roles drain their in-flight copies and
+// MMAs, TMEM is freed and the kernel returns.
 #include <algorithm>
 
 #include "tr_sm100.cuh"
@@ -47,38 +56,36 @@ constexpr int kD = 128;             // head dimension
 constexpr int BN = 64;              // keys per tile
 constexpr float kRescaleLog2 = 8.f; // O is rescaled only when the row maximum grows by more than this
 constexpr int kMaxB = 1024;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 template <int MT>
 struct Cfg {
-  static constexpr int STAGES = MT == 1 ? 3 : 2;
-  // MT == 1: two softmax warpgroups take alternate tiles, each with its own
-  // P buffer and O accumulator (combined at the end of a segment); MT == 2:
-  // one warpgroup per query head, one shared P buffer.
-  static constexpr int GROUPS = MT == 1 ? 2 : 1;
-  static constexpr int PB = MT == 1 ? 2 : 1;      // P buffers (hi + lo parts each)
+  static constexpr int KS = 4;                    // K ring stages
+  static constexpr int VS = MT == 1 ? 6 : 5;      // V ring stages
+  static constexpr int GROUPS = MT == 1 ? 2 : 1;  // softmax warpgroups sharing one query head
+  static constexpr int NSB = 4 / MT;              // S/P buffers in TMEM
   static constexpr int Q_HALF = 128 * 128;        // 128 rows x 64 bf16 (one d-half), bytes
   static constexpr int KV_HALF = 64 * 128;        // 64 keys x 64 bf16
   static constexpr int KV_TILE = 2 * KV_HALF;
-  static constexpr int P_PART = 128 * 128;        // 128 rows x 64 keys x 2 B
-  static constexpr int P_TILE = 2 * P_PART;       // hi, lo
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + MT * 2 * Q_HALF;
-  static constexpr int OFF_V = OFF_K + STAGES * KV_TILE;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_TILE;
-  static constexpr int OFF_BAR = OFF_P + PB * MT * P_TILE;
-  static constexpr int SOFT = 128 * MT * GROUPS;  // softmax threads
-  static constexpr int THREADS = 64 + SOFT;
+  static constexpr int OFF_V = OFF_K + KS * KV_TILE;
+  static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
+  static constexpr int SOFT = 256;                // softmax threads: two warpgroups
+  static constexpr int THREADS = 96 + SOFT;
   static constexpr uint32_t TMEM_COLS = 512;
-  __host__ __device__ static constexpr uint32_t s_col(int buf, int m) { return (uint32_t)((buf * MT + m) * BN); }
-  // accumulator o (0 .. MT*GROUPS-1) after the S buffers
-  __host__ __device__ static constexpr uint32_t o_col(int o) { return (uint32_t)(2 * MT * BN + o * kD); }
+  __host__ __device__ static constexpr uint32_t o_col(int o) { return (uint32_t)(o * kD); }
+  __host__ __device__ static constexpr uint32_t s_col(int buf, int m) { return (uint32_t)(2 * kD + (buf * MT + m) * BN); }
 };
+static_assert(Cfg<1>::s_col(Cfg<1>::NSB - 1, 0) + BN <= Cfg<1>::TMEM_COLS, "TMEM budget");
+static_assert(Cfg<2>::s_col(Cfg<2>::NSB - 1, 1) + BN <= Cfg<2>::TMEM_COLS, "TMEM budget");
 
-template <int S, int PB>
+template <int MT>
 struct Bars {
+  static constexpr int KS = Cfg<MT>::KS, VS = Cfg<MT>::VS, NSB = Cfg<MT>::NSB;
   uint64_t q_full, q_empty;
-  uint64_t k_full[S], k_empty[S], v_full[S], v_empty[S];
-  uint64_t s_full[2], s_empty[2], p_full[PB], pv_done[PB];
+  uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
+  uint64_t s_full[NSB], p_full[NSB], pv_done[NSB];
   uint64_t o_full, o_empty, drain, ml_ready;
   uint32_t tmem;
   int abort;
@@ -136,6 +143,30 @@ __device__ __forceinline__ Seg decode(long long t, long long t_lo, long long t_h
   return s;
 }
 
+// Walks a CTA's tiles segment by segment: u is the tile's index inside the
+// current segment, sc the segment's index inside the CTA.
+struct Cursor {
+  long long t;  // first tile of the current segment
+  Seg sg;
+  int u, sc;
+  __device__ __forceinline__ void init(long long t_lo, long long t_hi, const int *pref, const int *Ls,
+                                       const AttnArgs &a) {
+    t = t_lo;
+    u = 0;
+    sc = 0;
+    if (t < t_hi) sg = decode(t, t_lo, t_hi, pref, Ls, a);
+  }
+  __device__ __forceinline__ bool last() const { return u == sg.n - 1; }
+  __device__ __forceinline__ void advance(long long t_lo, long long t_hi, const int *pref, const int *Ls,
+                                          const AttnArgs &a) {
+    if (++u < sg.n) return;
+    t += sg.n;
+    u = 0;
+    ++sc;
+    if (t < t_hi) sg = decode(t, t_lo, t_hi, pref, Ls, a);
+  }
+};
+
 template <int MT>
 __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKc,
@@ -143,10 +174,10 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmVt, const AttnArgs a, const __grid_constant__ TreeDev tree) {
   using namespace sm100;
   using C = Cfg<MT>;
-  constexpr int S = C::STAGES, PB = C::PB;
+  constexpr int KS = C::KS, VS = C::VS, NSB = C::NSB, GROUPS = C::GROUPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  Bars<S, PB> *bars = (Bars<S, PB> *)(smem + C::OFF_BAR);
+  Bars<MT> *bars = (Bars<MT> *)(smem + C::OFF_BAR);
   volatile int *abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
@@ -154,17 +185,16 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->q_empty, 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NSB; ++b) {
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_empty[b], 128 * MT);
-    }
-    for (int b = 0; b < PB; ++b) {
       mbar_init(&bars->p_full[b], 128 * MT);
       mbar_init(&bars->pv_done[b], 1);
     }
@@ -208,70 +238,71 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     }
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------- producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------ producers
     if (lane == 0) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmKc);
-      tma_prefetch_desc(&tmVc);
-      tma_prefetch_desc(&tmKt);
-      tma_prefetch_desc(&tmVt);
-      int kc = 0, vc = 0, sc = 0;
-      int q_armed = -1, k_last[S], v_last[S];
-      for (int s = 0; s < S; ++s) k_last[s] = v_last[s] = -1;
+      const bool is_k = warp == 0;
+      constexpr int SMAX = KS > VS ? KS : VS;
+      const int NS = is_k ? KS : VS;
+      uint64_t *full = is_k ? bars->k_full : bars->v_full;
+      uint64_t *empty = is_k ? bars->k_empty : bars->v_empty;
+      const CUtensorMap *mc = is_k ? &tmKc : &tmVc;
+      const CUtensorMap *mt = is_k ? &tmKt : &tmVt;
+      uint8_t *ring = smem + (is_k ? C::OFF_K : C::OFF_V);
+      if (is_k) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmKc);
+        tma_prefetch_desc(&tmKt);
+      } else {
+        tma_prefetch_desc(&tmVc);
+        tma_prefetch_desc(&tmVt);
+      }
+      int cnt = 0, sc = 0, q_armed = -1, last[SMAX];
+      for (int s = 0; s < SMAX; ++s) last[s] = -1;
       bool ok = true;
       for (long long t = t_lo; t < t_hi && ok && !*abort; ++sc) {
         const Seg sg = decode(t, t_lo, t_hi, bars->pref, bars->Ls, a);
         t += sg.n;
-        if (!mbar_wait(&bars->q_empty, (sc & 1) ^ 1, abort)) {
-          give_up();
-          break;
+        if (is_k) {
+          if (!mbar_wait(&bars->q_empty, (sc & 1) ^ 1, abort)) {
+            give_up();
+            break;
+          }
+          mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(MT * 2 * a.q_rows * 128));
+          for (int m = 0; m < MT; ++m) {
+            const int h = sg.g * a.G + sg.hg * MT + m;
+            for (int half = 0; half < 2; ++half)
+              tma_load_3d(smem + C::OFF_Q + (m * 2 + half) * C::Q_HALF, &tmQ, &bars->q_full, half * 64, h, sg.b * N);
+          }
+          q_armed = sc & 1;
         }
-        mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(MT * 2 * a.q_rows * 128));
-        for (int m = 0; m < MT; ++m) {
-          const int h = sg.g * a.G + sg.hg * MT + m;
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(smem + C::OFF_Q + (m * 2 + half) * C::Q_HALF, &tmQ, &bars->q_full, half * 64, h, sg.b * N);
-        }
-        q_armed = sc & 1;
-        for (int u = 0; u < sg.n && ok; ++u) {
+        for (int u = 0; u < sg.n; ++u) {
           const int j = sg.j0 + u;
           const bool cache = j < sg.n_ct;
-          const int y_cache = (sg.b * a.Hkv + sg.g) * a.cap + j * BN;
-          const int node0 = (j - sg.n_ct) * BN;
-          for (int kv = 0; kv < 2; ++kv) {
-            int &cnt = kv ? vc : kc;
-            uint64_t *full = kv ? bars->v_full : bars->k_full;
-            uint64_t *empty = kv ? bars->v_empty : bars->k_empty;
-            int *last = kv ? v_last : k_last;
-            const int s = cnt % S;
-            const uint32_t ph = (cnt / S) & 1;
-            if (!mbar_wait(&empty[s], ph ^ 1, abort)) {
-              give_up();
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * (cache ? a.c_rows : a.t_rows) * 128));
-            uint8_t *dst = smem + (kv ? C::OFF_V : C::OFF_K) + s * C::KV_TILE;
-            for (int half = 0; half < 2; ++half) {
-              if (cache)
-                tma_load_2d(dst + half * C::KV_HALF, kv ? &tmVc : &tmKc, &full[s], half * 64, y_cache);
-              else
-                tma_load_3d(dst + half * C::KV_HALF, kv ? &tmVt : &tmKt, &full[s], half * 64, sg.g,
-                            sg.b * N + node0);
-            }
-            last[s] = (int)ph;
-            ++cnt;
+          const int s = cnt % NS;
+          const uint32_t ph = (cnt / NS) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort)) {
+            give_up();
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * (cache ? a.c_rows : a.t_rows) * 128));
+          uint8_t *dst = ring + s * C::KV_TILE;
+          for (int half = 0; half < 2; ++half) {
+            if (cache)
+              tma_load_2d(dst + half * C::KV_HALF, mc, &full[s], half * 64, (sg.b * a.Hkv + sg.g) * a.cap + j * BN);
+            else
+              tma_load_3d(dst + half * C::KV_HALF, mt, &full[s], half * 64, sg.g, sg.b * N + (j - sg.n_ct) * BN);
+          }
+          last[s] = (int)ph;
+          ++cnt;
         }
       }
       if (*abort) {
         // let the copies already issued land before the CTA can exit
         if (q_armed >= 0) mbar_drain(&bars->q_full, (uint32_t)q_armed);
-        for (int s = 0; s < S; ++s) {
-          if (k_last[s] >= 0) mbar_drain(&bars->k_full[s], (uint32_t)k_last[s]);
-          if (v_last[s] >= 0) mbar_drain(&bars->v_full[s], (uint32_t)v_last[s]);
-        }
+        for (int s = 0; s < NS; ++s)
+          if (last[s] >= 0) mbar_drain(&full[s], (uint32_t)last[s]);
       }
     }
   } else if (warp == 1) {
@@ -279,95 +310,82 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BN);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kD, true);
-      int kc = 0, vc = 0, gt = 0, sc = 0;
-      bool ok = true;
-      for (long long t = t_lo; t < t_hi && ok && !*abort; ++sc) {
-        const Seg sg = decode(t, t_lo, t_hi, bars->pref, bars->Ls, a);
-        t += sg.n;
-        const int T = sg.n;
-        if (!mbar_wait(&bars->q_full, sc & 1, abort)) {
-          give_up();
-          break;
+      const int n_all = (int)(t_hi - t_lo);
+      Cursor cq, cp;  // the QK and the PV streams
+      cq.init(t_lo, t_hi, bars->pref, bars->Ls, a);
+      cp.init(t_lo, t_hi, bars->pref, bars->Ls, a);
+      int qi = 0, pi = 0, idle = 0;
+      uint64_t idle_since = 0;
+      while (pi < n_all) {
+        bool progress = false;
+        // S = Q.K^T of tile qi: its Q, its K stage, and an S/P buffer whose
+        // previous PV product has completed
+        if (qi < n_all) {
+          const int sb = qi % NSB, ks_ = qi % KS;
+          if ((cq.u != 0 || mbar_test(&bars->q_full, cq.sc & 1)) && mbar_test(&bars->k_full[ks_], (qi / KS) & 1) &&
+              (qi < NSB || mbar_test(&bars->pv_done[sb], ((qi / NSB) - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t kb = smem_u32(smem + C::OFF_K + ks_ * C::KV_TILE);
+            for (int m = 0; m < MT; ++m) {
+              const uint32_t qb = smem_u32(smem + C::OFF_Q + m * 2 * C::Q_HALF);
+#pragma unroll
+              for (int k = 0; k < kD / 16; ++k)
+                mma_bf16(tmem + C::s_col(sb, m), desc_kmajor_sw128(qb + (k >> 2) * C::Q_HALF + (k & 3) * 32),
+                         desc_kmajor_sw128(kb + (k >> 2) * C::KV_HALF + (k & 3) * 32), kIdescQK, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars->k_empty[ks_]);
+            mma_commit(&bars->s_full[sb]);
+            if (cq.last()) mma_commit(&bars->q_empty);
+            cq.advance(t_lo, t_hi, bars->pref, bars->Ls, a);
+            ++qi;
+            progress = true;
+          }
         }
-        tc_fence_after();
-        // S = Q.K^T of tile u of the segment, once its S buffer has been read
-        // by the softmax of the tile two before it
-        auto issue_qk = [&](int u) -> bool {
-          const int gq = gt + u, sb = gq & 1;
-          if (gq >= 2 && !mbar_wait(&bars->s_empty[sb], ((gq - 2) >> 1) & 1, abort)) return false;
-          const int s = kc % S;
-          if (!mbar_wait(&bars->k_full[s], (kc / S) & 1, abort)) return false;
-          tc_fence_after();
-          const uint32_t kb = smem_u32(smem + C::OFF_K + s * C::KV_TILE);
-          for (int m = 0; m < MT; ++m) {
-            const uint32_t qb = smem_u32(smem + C::OFF_Q + m * 2 * C::Q_HALF);
+        // O += P.V of tile pi: its P, its V stage, and (first tile of a
+        // segment) an accumulator the previous segment's epilogue has read
+        if (pi < qi) {
+          const int sb = pi % NSB, vs_ = pi % VS;
+          if (mbar_test(&bars->p_full[sb], (pi / NSB) & 1) && mbar_test(&bars->v_full[vs_], (pi / VS) & 1) &&
+              (cp.u != 0 || mbar_test(&bars->o_empty, (cp.sc & 1) ^ 1))) {
+            tc_fence_after();
+            const uint32_t vb = smem_u32(smem + C::OFF_V + vs_ * C::KV_TILE);
+            const int j = cp.u;
+            for (int m = 0; m < MT; ++m) {
+              const int o = MT == 1 ? (pi & 1) : m;  // MT == 1: the tile's warpgroup owns accumulator pi & 1
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks)
-              mma_bf16(tmem + C::s_col(sb, m), desc_kmajor_sw128(qb + (ks >> 2) * C::Q_HALF + (ks & 3) * 32),
-                       desc_kmajor_sw128(kb + (ks >> 2) * C::KV_HALF + (ks & 3) * 32), kIdescQK, ks > 0 ? 1u : 0u);
-          }
-          mma_commit(&bars->k_empty[s]);
-          mma_commit(&bars->s_full[sb]);
-          if (u == T - 1) mma_commit(&bars->q_empty);
-          ++kc;
-          return true;
-        };
-        for (int u = 0; u < T && u < 2 && ok; ++u)
-          if (!issue_qk(u)) {
-            give_up();
-            ok = false;
-          }
-        for (int j = 0; j < T && ok; ++j) {
-          if (j + 2 < T && !issue_qk(j + 2)) {
-            give_up();
-            ok = false;
-            break;
-          }
-          // O += P.V of tile j
-          const int gj = gt + j, pb = gj % PB;
-          if (!mbar_wait(&bars->p_full[pb], (gj / PB) & 1, abort)) {
-            give_up();
-            ok = false;
-            break;
-          }
-          const int s = vc % S;
-          if (!mbar_wait(&bars->v_full[s], (vc / S) & 1, abort)) {
-            give_up();
-            ok = false;
-            break;
-          }
-          if (j == 0 && !mbar_wait(&bars->o_empty, (sc & 1) ^ 1, abort)) {
-            give_up();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t vb = smem_u32(smem + C::OFF_V + s * C::KV_TILE);
-          for (int m = 0; m < MT; ++m) {
-            const uint32_t pbase = smem_u32(smem + C::OFF_P + (pb * MT + m) * C::P_TILE);
-            const int o = MT == 1 ? (gj & 1) : m;  // MT == 1: the tile's warpgroup owns accumulator gj & 1
+              for (int part = 0; part < 2; ++part)
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-              for (int ks = 0; ks < BN / 16; ++ks)
-                mma_bf16(tmem + C::o_col(o), desc_kmajor_sw128(pbase + part * C::P_PART + ks * 32),
-                         desc_mnmajor_sw128(vb + ks * 2048, C::KV_HALF), kIdescPV,
-                         (j >= C::GROUPS || part > 0 || ks > 0) ? 1u : 0u);
+                for (int k = 0; k < BN / 16; ++k)
+                  mma_bf16_ts(tmem + C::o_col(o), tmem + C::s_col(sb, m) + part * 32 + k * 8,
+                              desc_mnmajor_sw128(vb + k * 2048, C::KV_HALF), kIdescPV,
+                              (j >= GROUPS || part > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->v_empty[vs_]);
+            mma_commit(&bars->pv_done[sb]);
+            if (cp.last()) mma_commit(&bars->o_full);
+            cp.advance(t_lo, t_hi, bars->pref, bars->Ls, a);
+            ++pi;
+            progress = true;
           }
-          mma_commit(&bars->v_empty[s]);
-          mma_commit(&bars->pv_done[pb]);
-          ++vc;
         }
-        if (!ok) break;
-        mma_commit(&bars->o_full);
-        gt += T;
+        if (progress) {
+          idle = 0;
+        } else if ((++idle & 63) == 0) {
+          if (*abort) break;
+          const uint64_t now = globaltimer_ns();
+          if (idle == 64) idle_since = now;
+          else if (now - idle_since > kWaitLimitNs) {
+            give_up();
+            break;
+          }
+        }
       }
       mma_commit(&bars->drain);
       mbar_drain(&bars->drain, 0);
     }
   } else {
     // -------------------------------------------------------------- softmax
-    const int su = (warp - 2) >> 2;            // softmax unit: warpgroup (MT == 1) or query head (MT == 2)
+    const int su = (warp - 3) >> 2;            // softmax unit: warpgroup (MT == 1) or query head (MT == 2)
     const int grp = MT == 1 ? su : 0;
     const int mt = MT == 1 ? 0 : su;
     const int oacc = su;                       // this unit's O accumulator
@@ -378,7 +396,6 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     const int rn = row_valid ? r : 0;
     const unsigned long long anc0 = tree.anc[rn][0], anc1 = tree.anc[rn][1];
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    uint8_t *prow_base = smem + C::OFF_P + mt * C::P_TILE + (r >> 3) * 1024 + (r & 7) * 128;
     // every wait of this role is warp-uniform: a lane that gives up takes its
     // whole warp with it, so the warp-collective TMEM accesses stay converged
     auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -397,28 +414,19 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       float m_run = -INFINITY, l_run = 0.f;
       int done_here = 0;  // tiles of this segment this unit has folded into its accumulator
       for (int u = 0; u < T && ok; ++u) {
-        const int gtt = gt + u, sb = gtt & 1, pb = gtt % PB;
+        const int gtt = gt + u, sb = gtt % NSB;
         if (MT == 1 && (gtt & 1) != grp) continue;  // the other warpgroup's tile
-        if (!wwait(&bars->s_full[sb], (gtt >> 1) & 1)) {
+        // also for inactive warps: their p_full arrival must not run ahead
+        // into the buffer's next use
+        if (!wwait(&bars->s_full[sb], (gtt / NSB) & 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (!warp_active) mbar_arrive(&bars->s_empty[sb]);
         if (warp_active) {
+          const uint32_t scol = tmem + lane_off + C::s_col(sb, mt);
           float sv[BN];
-          {
-            float tmp[32];
-            tmem_ld32(tmem + lane_off + C::s_col(sb, mt), tmp);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) sv[c] = tmp[c];
-            tmem_ld32(tmem + lane_off + C::s_col(sb, mt) + 32, tmp);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) sv[32 + c] = tmp[c];
-          }
-          // S is in registers: the MMA may overwrite this buffer with the next tile's scores
-          tc_fence_before();
-          mbar_arrive(&bars->s_empty[sb]);
+          tmem_ld64(scol, sv);
           const int j = sg.j0 + u;
           const bool cache = j < sg.n_ct;
           const int key0 = j * BN;
@@ -452,8 +460,8 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           const bool need = m_new > m_run + kRescaleLog2;  // also true for the row's first finite maximum
           if (__any_sync(0xffffffffu, need && done_here > 0)) {
             // O already holds this unit's earlier tiles: wait for the last PV into it, then scale it
-            const int gp = gtt - PB;
-            if (!wwait(&bars->pv_done[gp % PB], (gp / PB) & 1)) {
+            const int gp = gtt - GROUPS;
+            if (!wwait(&bars->pv_done[gp % NSB], (gp / NSB) & 1)) {
               ok = false;
               break;
             }
@@ -472,39 +480,34 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
             l_run = m_run == -INFINITY ? 0.f : l_run * ex2(m_run - m_new);
             m_run = m_new;
           }
-          // this P buffer is free once the PV that last read it is done
-          if (gtt >= PB && !wwait(&bars->pv_done[pb], ((gtt - PB) / PB) & 1)) {
-            ok = false;
-            break;
-          }
-          uint8_t *prow = prow_base + pb * MT * C::P_TILE;
           // ex2(-inf) = 0 for masked keys; a row that has seen no visible key yet
           // (m_run = -inf, all its keys masked) subtracts 0 instead of -inf
           const float m_sub = m_run == -INFINITY ? 0.f : m_run;
           float l4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+          // P over the S columns just read: hi parts in the first 32, lo in the next 32
 #pragma unroll
-          for (int c8 = 0; c8 < BN / 8; ++c8) {
-            uint32_t whi[4], wlo[4];
+          for (int half = 0; half < 2; ++half) {
+            uint32_t whi[16], wlo[16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float p0 = ex2(sv[c8 * 8 + 2 * q] - m_sub);
-              const float p1 = ex2(sv[c8 * 8 + 2 * q + 1] - m_sub);
-              l4[q] += p0 + p1;
+            for (int q = 0; q < 16; ++q) {
+              const int c = half * 32 + 2 * q;
+              const float p0 = ex2(sv[c] - m_sub);
+              const float p1 = ex2(sv[c + 1] - m_sub);
+              l4[q & 3] += p0 + p1;
               const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
               const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(hi), p1 - __high2float(hi));
               whi[q] = *reinterpret_cast<const uint32_t *>(&hi);
               wlo[q] = *reinterpret_cast<const uint32_t *>(&lo);
             }
-            const int off = (c8 ^ (r & 7)) << 4;
-            *reinterpret_cast<uint4 *>(prow + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-            *reinterpret_cast<uint4 *>(prow + C::P_PART + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+            tmem_st16_nowait(scol + half * 16, whi);
+            tmem_st16_nowait(scol + 32 + half * 16, wlo);
           }
+          tmem_wait_st();
           l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-          fence_proxy_async_smem();
         }
         ++done_here;
         tc_fence_before();
-        mbar_arrive(&bars->p_full[pb]);
+        mbar_arrive(&bars->p_full[sb]);
       }
       if (!ok) break;
       // ---- end of the segment: normalised output or a partial
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a, int M
 
 template <int MT>
 size_t smem_bytes() {
-  return (size_t)Cfg<MT>::OFF_BAR + sizeof(Bars<Cfg<MT>::STAGES, Cfg<MT>::PB>) + 1024;
+  return (size_t)Cfg<MT>::OFF_BAR + sizeof(Bars<MT>) + 1024;
 }
 
 struct Plan {
