@@ -14,19 +14,20 @@
 // boundary leaves (m, l, O) partials in two slots per CTA, and a small second
 // kernel merges them.
 //
-// Per CTA:
+// Per CTA (12 warps, so each SM sub-partition hosts one helper warp and two
+// softmax warps):
 //   warp 0      TMA producer of Q (3-D map over [B*N, Hq, d]) and of the K
 //               ring: tiles of 64 keys from the cache (2-D map over
 //               [B*Hkv*cap, d]) or the tree (3-D map over [B*N, Hkv, d]);
 //   warp 2      TMA producer of the V ring, same maps for V; the two rings
 //               run independently, so a V stage still held by a PV product
 //               never stops the K stream;
-//   warp 1      one thread issues tcgen05.mma as the operands become ready
-//               (non-blocking polls, so neither stream waits behind the
-//               other): S = Q.K^T (M128 x N64 x K128, fp32 in TMEM) and
-//               O += P.V (M128 x N128 x K64) with P read from TMEM and V
-//               from shared memory as an MN-major operand;
-//   warps 3..   softmax, one query row per thread (one TMEM lane): the mask
+//   warp 1      issues S = Q.K^T (tcgen05.mma M128 x N64 x K128, fp32 in TMEM);
+//   warp 3      issues O += P.V (M128 x N128 x K64) with P read from TMEM and V
+//               from shared memory as an MN-major operand.  Two issuers keep
+//               each one's instruction stream short; both run warp-uniformly
+//               and issue from one elected lane;
+//   warps 4..11 softmax, one query row per thread (one TMEM lane): the mask
 //               (key < L for the cache, ancestor bit for the tree), exp2 with a
 //               running maximum that only rescales O when it grows by more
 //               than 2^8, and P written back over the S columns it came from.
@@ -56,7 +57,6 @@ constexpr int kD = 128;             // head dimension
 constexpr int BN = 64;              // keys per tile
 constexpr float kRescaleLog2 = 8.f; // O is rescaled only when the row maximum grows by more than this
 constexpr int kMaxB = 1024;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 template <int MT>
 struct Cfg {
@@ -72,7 +72,7 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + KS * KV_TILE;
   static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
   static constexpr int SOFT = 256;                // softmax threads: two warpgroups
-  static constexpr int THREADS = 96 + SOFT;
+  static constexpr int THREADS = 128 + SOFT;
   static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t o_col(int o) { return (uint32_t)(o * kD); }
   __host__ __device__ static constexpr uint32_t s_col(int buf, int m) { return (uint32_t)(2 * kD + (buf * MT + m) * BN); }
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     }
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, C::SOFT);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);  // one commit from each MMA issuer
     mbar_init(&bars->ml_ready, 128);
     bars->abort = 0;
     fence_mbar_init();
@@ -236,6 +236,15 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       *abort = 1;
       tr_flag(a.status, TR_DEV_TIMEOUT);
     }
+  };
+
+  // every wait of the warp-wide roles is warp-uniform: a lane that gives up
+  // takes its whole warp with it, so warp-collective instructions stay converged
+  auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+    const bool mine = mbar_wait(bar, parity, abort);
+    const bool all = __all_sync(0xffffffffu, mine);
+    if (!all) give_up();
+    return all;
   };
 
   if (warp == 0 || warp == 2) {
@@ -306,86 +315,86 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(128, BN);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(128, kD, true);
-      const int n_all = (int)(t_hi - t_lo);
-      Cursor cq, cp;  // the QK and the PV streams
-      cq.init(t_lo, t_hi, bars->pref, bars->Ls, a);
-      cp.init(t_lo, t_hi, bars->pref, bars->Ls, a);
-      int qi = 0, pi = 0, idle = 0;
-      uint64_t idle_since = 0;
-      while (pi < n_all) {
-        bool progress = false;
-        // S = Q.K^T of tile qi: its Q, its K stage, and an S/P buffer whose
-        // previous PV product has completed
-        if (qi < n_all) {
-          const int sb = qi % NSB, ks_ = qi % KS;
-          if ((cq.u != 0 || mbar_test(&bars->q_full, cq.sc & 1)) && mbar_test(&bars->k_full[ks_], (qi / KS) & 1) &&
-              (qi < NSB || mbar_test(&bars->pv_done[sb], ((qi / NSB) - 1) & 1))) {
-            tc_fence_after();
-            const uint32_t kb = smem_u32(smem + C::OFF_K + ks_ * C::KV_TILE);
-            for (int m = 0; m < MT; ++m) {
-              const uint32_t qb = smem_u32(smem + C::OFF_Q + m * 2 * C::Q_HALF);
+    // ------------------------------------------------------------- QK issuer
+    // S = Q.K^T of tile i once its Q and K have landed and the S/P buffer's
+    // previous PV product has completed.  The whole warp runs the loop, so its
+    // control flow and operands stay warp-uniform; one elected lane issues.
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
+    const uint64_t dq0 = desc_kmajor_sw128(smem_u32(smem + C::OFF_Q));
+    const uint64_t dk0 = desc_kmajor_sw128(smem_u32(smem + C::OFF_K));
+    Cursor cq;
+    cq.init(t_lo, t_hi, bars->pref, bars->Ls, a);
+    const int n_all = (int)(t_hi - t_lo);
+    for (int i = 0; i < n_all; ++i) {
+      const int sb = i % NSB, ks = i % KS;
+      if (cq.u == 0 && !wwait(&bars->q_full, cq.sc & 1)) break;
+      if (!wwait(&bars->k_full[ks], (i / KS) & 1)) break;
+      if (i >= NSB && !wwait(&bars->pv_done[sb], ((i / NSB) - 1) & 1)) break;
+      tc_fence_after();
+      if (elect_one()) {
+        // descriptor start addresses count 16-byte units
+        const uint64_t dk = dk0 + (uint64_t)(ks * (C::KV_TILE >> 4));
 #pragma unroll
-              for (int k = 0; k < kD / 16; ++k)
-                mma_bf16(tmem + C::s_col(sb, m), desc_kmajor_sw128(qb + (k >> 2) * C::Q_HALF + (k & 3) * 32),
-                         desc_kmajor_sw128(kb + (k >> 2) * C::KV_HALF + (k & 3) * 32), kIdescQK, k > 0 ? 1u : 0u);
-            }
-            mma_commit(&bars->k_empty[ks_]);
-            mma_commit(&bars->s_full[sb]);
-            if (cq.last()) mma_commit(&bars->q_empty);
-            cq.advance(t_lo, t_hi, bars->pref, bars->Ls, a);
-            ++qi;
-            progress = true;
-          }
-        }
-        // O += P.V of tile pi: its P, its V stage, and (first tile of a
-        // segment) an accumulator the previous segment's epilogue has read
-        if (pi < qi) {
-          const int sb = pi % NSB, vs_ = pi % VS;
-          if (mbar_test(&bars->p_full[sb], (pi / NSB) & 1) && mbar_test(&bars->v_full[vs_], (pi / VS) & 1) &&
-              (cp.u != 0 || mbar_test(&bars->o_empty, (cp.sc & 1) ^ 1))) {
-            tc_fence_after();
-            const uint32_t vb = smem_u32(smem + C::OFF_V + vs_ * C::KV_TILE);
-            const int j = cp.u;
-            for (int m = 0; m < MT; ++m) {
-              const int o = MT == 1 ? (pi & 1) : m;  // MT == 1: the tile's warpgroup owns accumulator pi & 1
+        for (int m = 0; m < MT; ++m) {
+          const uint64_t dq = dq0 + (uint64_t)(m * (2 * C::Q_HALF >> 4));
 #pragma unroll
-              for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int k = 0; k < BN / 16; ++k)
-                  mma_bf16_ts(tmem + C::o_col(o), tmem + C::s_col(sb, m) + part * 32 + k * 8,
-                              desc_mnmajor_sw128(vb + k * 2048, C::KV_HALF), kIdescPV,
-                              (j >= GROUPS || part > 0 || k > 0) ? 1u : 0u);
-            }
-            mma_commit(&bars->v_empty[vs_]);
-            mma_commit(&bars->pv_done[sb]);
-            if (cp.last()) mma_commit(&bars->o_full);
-            cp.advance(t_lo, t_hi, bars->pref, bars->Ls, a);
-            ++pi;
-            progress = true;
-          }
+          for (int k = 0; k < kD / 16; ++k)
+            mma_bf16(tmem + C::s_col(sb, m), dq + (uint64_t)(((k >> 2) * C::Q_HALF + (k & 3) * 32) >> 4),
+                     dk + (uint64_t)(((k >> 2) * C::KV_HALF + (k & 3) * 32) >> 4), kIdesc, k > 0 ? 1u : 0u);
         }
-        if (progress) {
-          idle = 0;
-        } else if ((++idle & 63) == 0) {
-          if (*abort) break;
-          const uint64_t now = globaltimer_ns();
-          if (idle == 64) idle_since = now;
-          else if (now - idle_since > kWaitLimitNs) {
-            give_up();
-            break;
-          }
-        }
+        mma_commit(&bars->k_empty[ks]);
+        mma_commit(&bars->s_full[sb]);
+        if (cq.last()) mma_commit(&bars->q_empty);
       }
-      mma_commit(&bars->drain);
-      mbar_drain(&bars->drain, 0);
+      __syncwarp();
+      cq.advance(t_lo, t_hi, bars->pref, bars->Ls, a);
     }
+    if (elect_one()) mma_commit(&bars->drain);
+    __syncwarp();
+    mbar_drain(&bars->drain, 0);
+  } else if (warp == 3) {
+    // ------------------------------------------------------------- PV issuer
+    // O += P.V of tile i once its P is in TMEM and its V has landed; the first
+    // tile of a segment also waits for the previous segment's epilogue to have
+    // read the accumulators.
+    constexpr uint32_t kIdesc = idesc_bf16_f32(128, kD, true);
+    const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(smem + C::OFF_V), C::KV_HALF);
+    Cursor cp;
+    cp.init(t_lo, t_hi, bars->pref, bars->Ls, a);
+    const int n_all = (int)(t_hi - t_lo);
+    for (int i = 0; i < n_all; ++i) {
+      const int sb = i % NSB, vs = i % VS;
+      if (cp.u == 0 && !wwait(&bars->o_empty, (cp.sc & 1) ^ 1)) break;
+      if (!wwait(&bars->p_full[sb], (i / NSB) & 1)) break;
+      if (!wwait(&bars->v_full[vs], (i / VS) & 1)) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t dv = dv0 + (uint64_t)(vs * (C::KV_TILE >> 4));
+        const uint32_t first = cp.u >= GROUPS ? 1u : 0u;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const uint32_t d_o = tmem + C::o_col(MT == 1 ? (i & 1) : m);  // MT == 1: tile i's warpgroup owns accumulator i & 1
+          const uint32_t a_p = tmem + C::s_col(sb, m);
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+              mma_bf16_ts(d_o, a_p + part * 32 + k * 8, dv + (uint64_t)(k * (2048 >> 4)), kIdesc,
+                          (part > 0 || k > 0) ? 1u : first);
+        }
+        mma_commit(&bars->v_empty[vs]);
+        mma_commit(&bars->pv_done[sb]);
+        if (cp.last()) mma_commit(&bars->o_full);
+      }
+      __syncwarp();
+      cp.advance(t_lo, t_hi, bars->pref, bars->Ls, a);
+    }
+    if (elect_one()) mma_commit(&bars->drain);
+    __syncwarp();
+    mbar_drain(&bars->drain, 0);
   } else {
     // -------------------------------------------------------------- softmax
-    const int su = (warp - 3) >> 2;            // softmax unit: warpgroup (MT == 1) or query head (MT == 2)
+    const int su = (warp - 4) >> 2;            // softmax unit: warpgroup (MT == 1) or query head (MT == 2)
     const int grp = MT == 1 ? su : 0;
     const int mt = MT == 1 ? 0 : su;
     const int oacc = su;                       // this unit's O accumulator
@@ -396,14 +405,6 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     const int rn = row_valid ? r : 0;
     const unsigned long long anc0 = tree.anc[rn][0], anc1 = tree.anc[rn][1];
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    // every wait of this role is warp-uniform: a lane that gives up takes its
-    // whole warp with it, so the warp-collective TMEM accesses stay converged
-    auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
-      const bool mine = mbar_wait(bar, parity, abort);
-      const bool all = __all_sync(0xffffffffu, mine);
-      if (!all) give_up();
-      return all;
-    };
     int gt = 0, sc = 0;
     bool ok = true;
     for (long long t = t_lo; t < t_hi && ok; ++sc) {
