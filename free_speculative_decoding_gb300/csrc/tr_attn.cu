@@ -89,7 +89,7 @@ struct Bars {
   uint64_t o_full, o_empty, drain, ml_ready;
   uint32_t tmem;
   int abort;
-  float2 ml_x[2][128];  // second warpgroup's (m, l) per row, by segment parity
+  float2 ml_x[2][2][128];  // each warpgroup's (m, l) per row, by segment parity (MT == 1)
   int Ls[kMaxB];
   int pref[kMaxB + 1];  // first tile of sequence b in the global tile order
 };
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_empty, C::SOFT);
     mbar_init(&bars->drain, 2);  // one commit from each MMA issuer
-    mbar_init(&bars->ml_ready, 128);
+    mbar_init(&bars->ml_ready, 256);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       t += sg.n;
       const int T = sg.n;
       const int h = sg.g * a.G + sg.hg * MT + mt;
-      float m_run = -INFINITY, l_run = 0.f;
+      float m_run = -INFINITY, l_run = 0.f;  // running maximum (log2 units) and sum
       int done_here = 0;  // tiles of this segment this unit has folded into its accumulator
       for (int u = 0; u < T && ok; ++u) {
         const int gtt = gt + u, sb = gtt % NSB;
@@ -431,32 +431,28 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           const int j = sg.j0 + u;
           const bool cache = j < sg.n_ct;
           const int key0 = j * BN;
-          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
-          if (cache && key0 + BN <= sg.Lb) {
-            // a full cache tile: every key is visible (rows past N are never stored)
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-              sv[c] *= a.scale_log2;
-              mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+          if (!(cache && key0 + BN <= sg.Lb)) {
+            // a tile with invisible keys (the cache's last tile, the tree
+            // tiles): -inf where the validity mask has a zero.  A full cache
+            // tile needs none (its rows past N are never stored).
+            unsigned long long vm;
+            if (cache) {
+              vm = (1ull << (sg.Lb - key0)) - 1;  // 1 <= Lb - key0 < 64 here
+            } else {
+              const int node0 = (j - sg.n_ct) * BN, nv = N - node0;
+              vm = (node0 == 0 ? anc0 : anc1) & (nv >= 64 ? ~0ull : (1ull << nv) - 1);
             }
-          } else {
-            const int node0 = (j - sg.n_ct) * BN;
+            if (!row_valid) vm = 0;
+            const uint32_t vlo = (uint32_t)vm, vhi = (uint32_t)(vm >> 32);
 #pragma unroll
-            for (int c = 0; c < BN; ++c) {
-              bool valid;
-              if (cache) {
-                valid = key0 + c < sg.Lb;
-              } else {
-                const int nd = node0 + c;
-                const unsigned long long w = nd < 64 ? anc0 : anc1;
-                valid = nd < N && ((w >> (nd & 63)) & 1ull);
-              }
-              valid = valid && row_valid;
-              sv[c] = valid ? sv[c] * a.scale_log2 : -INFINITY;
-              mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
-            }
+            for (int c = 0; c < BN; ++c)
+              if (!(((c < 32 ? vlo : vhi) >> (c & 31)) & 1u)) sv[c] = -INFINITY;
           }
-          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
+#pragma unroll
+          for (int c = 0; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+          // the scale is positive, so the maximum of the raw scores scales to the scaled maximum
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
           const float m_new = fmaxf(m_run, mx);
           const bool need = m_new > m_run + kRescaleLog2;  // also true for the row's first finite maximum
           if (__any_sync(0xffffffffu, need && done_here > 0)) {
@@ -492,8 +488,8 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               const int c = half * 32 + 2 * q;
-              const float p0 = ex2(sv[c] - m_sub);
-              const float p1 = ex2(sv[c + 1] - m_sub);
+              const float p0 = ex2(fmaf(sv[c], a.scale_log2, -m_sub));
+              const float p1 = ex2(fmaf(sv[c + 1], a.scale_log2, -m_sub));
               l4[q & 3] += p0 + p1;
               const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
               const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(hi), p1 - __high2float(hi));
@@ -512,54 +508,63 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       }
       if (!ok) break;
       // ---- end of the segment: normalised output or a partial
+      if (!done_here) {
+        m_run = -INFINITY;
+        l_run = 0.f;
+      }
+      float2 other = make_float2(-INFINITY, 0.f);
+      if (MT == 1) {
+        // both warpgroups publish their (m, l); each then finishes half of the d columns
+        bars->ml_x[sc & 1][grp][r] = make_float2(m_run, l_run);
+        mbar_arrive(&bars->ml_ready);
+      }
       if (!wwait(&bars->o_full, sc & 1)) break;
       tc_fence_after();
-      if (MT == 1 && grp == 1) {
-        // hand this warpgroup's (m, l) to the first warpgroup, which combines the two accumulators
-        bars->ml_x[sc & 1][r] = make_float2(done_here ? m_run : -INFINITY, done_here ? l_run : 0.f);
-        mbar_arrive(&bars->ml_ready);
-      } else {
-        float2 other = make_float2(-INFINITY, 0.f);
-        if (MT == 1) {
-          if (!wwait(&bars->ml_ready, sc & 1)) break;
-          other = bars->ml_x[sc & 1][r];
-        }
-        if (!done_here) {
-          m_run = -INFINITY;
-          l_run = 0.f;
-        }
-        const float M = fmaxf(m_run, other.x);
-        const float wa = m_run == -INFINITY ? 0.f : ex2(m_run - M);
-        const float wb = other.x == -INFINITY ? 0.f : ex2(other.x - M);
-        const float l = l_run * wa + other.y * wb;
-        if (warp_active) {
-          const int slot = blockIdx.x * 2 + (sg.first_of_cta ? 0 : 1);
-          const long long prow_idx = ((long long)slot * MT + mt) * N + r;
-          const float scale_out = sg.complete ? (row_valid && l > 0.f ? 1.f / l : 0.f) : 1.f;
-          const bool use_a = wa != 0.f, use_b = MT == 1 && wb != 0.f;
-          float *dst = sg.complete ? a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD : a.part_o + prow_idx * kD;
-#pragma unroll 1
-          for (int c0 = 0; c0 < kD; c0 += 32) {
-            float oa[32], ob[32];
-            tmem_ld32(tmem + lane_off + C::o_col(oacc) + c0, oa);
-            if (MT == 1) tmem_ld32(tmem + lane_off + C::o_col(1) + c0, ob);
-            if (row_valid) {
-#pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                float v = use_a ? oa[c] * wa : 0.f;
-                if (use_b) v += ob[c] * wb;
-                oa[c] = v * scale_out;
-              }
-#pragma unroll
-              for (int c = 0; c < 32; c += 4)
-                *reinterpret_cast<float4 *>(dst + c0 + c) = make_float4(oa[c], oa[c + 1], oa[c + 2], oa[c + 3]);
-            }
-          }
-          if (!sg.complete && row_valid) a.part_ml[prow_idx] = make_float2(M, l);
-        }
+      if (MT == 1) {
+        if (!wwait(&bars->ml_ready, sc & 1)) break;
+        other = bars->ml_x[sc & 1][grp ^ 1][r];
       }
-      tc_fence_before();
-      mbar_arrive(&bars->o_empty);
+      const float M = fmaxf(m_run, other.x);
+      const float wa = m_run == -INFINITY ? 0.f : ex2(m_run - M);   // this unit's accumulator
+      const float wb = other.x == -INFINITY ? 0.f : ex2(other.x - M);  // the other warpgroup's (MT == 1)
+      const float l = l_run * wa + other.y * wb;
+      constexpr int COLS = MT == 1 ? kD / 2 : kD;  // columns this unit finishes
+      const int col0 = MT == 1 ? grp * COLS : 0;
+      if (warp_active) {
+        const int slot = blockIdx.x * 2 + (sg.first_of_cta ? 0 : 1);
+        const long long prow_idx = ((long long)slot * MT + mt) * N + r;
+        const float scale_out = sg.complete ? (row_valid && l > 0.f ? 1.f / l : 0.f) : 1.f;
+        // MT == 1: fold accumulator 0 with weight w0 and accumulator 1 with w1
+        const float w0 = MT == 1 ? (grp == 0 ? wa : wb) : wa;
+        const float w1 = MT == 1 ? (grp == 0 ? wb : wa) : 0.f;
+        float *dst = sg.complete ? a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD : a.part_o + prow_idx * kD;
+#pragma unroll 1
+        for (int c0 = col0; c0 < col0 + COLS; c0 += 32) {
+          float oa[32], ob[32];
+          tmem_ld32(tmem + lane_off + C::o_col(MT == 1 ? 0 : oacc) + c0, oa);
+          if (MT == 1) tmem_ld32(tmem + lane_off + C::o_col(1) + c0, ob);
+          if (c0 + 32 == col0 + COLS) {
+            // the last read of the accumulators: the next segment's PV may overwrite them
+            tc_fence_before();
+            mbar_arrive(&bars->o_empty);
+          }
+          if (row_valid) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              float v = w0 != 0.f ? oa[c] * w0 : 0.f;
+              if (MT == 1 && w1 != 0.f) v += ob[c] * w1;
+              oa[c] = v * scale_out;
+            }
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<float4 *>(dst + c + c0) = make_float4(oa[c], oa[c + 1], oa[c + 2], oa[c + 3]);
+          }
+        }
+        if (!sg.complete && row_valid && (MT == 2 || grp == 0)) a.part_ml[prow_idx] = make_float2(M, l);
+      } else {
+        tc_fence_before();
+        mbar_arrive(&bars->o_empty);
+      }
       gt += T;
     }
   }
@@ -668,7 +673,7 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
                               const int32_t *L, int cap, int B, int Hq, int Hkv, int d, float scale,
                               const struct tr_tree *tree, float *O, void *ws, size_t ws_bytes, tr_stream_t stream) {
   if (!Q || !Kt || !Vt || !Kc || !Vc || !L || !tree || !O || B < 1 || Hq < 1 || Hkv < 1 || cap < 0) return TR_E_INVAL;
-  if (Hq % Hkv) return TR_E_INVAL;
+  if (Hq % Hkv || !(scale > 0.f) || !(scale < INFINITY)) return TR_E_INVAL;
   if (d != kD) return TR_E_UNSUPPORTED;
   const int N = tree->dev.N;
   // the global tile count must fit in 31 bits

@@ -148,9 +148,14 @@ int tr_retrieve(const void *M, tr_itype mtype, int B, int64_t V, int K, const st
  *   Kc, Vc [B, Hkv, cap, d] bf16, the first L[b] positions valid
  *   L      [B] int32 (device), 0 <= L[b] <= cap
  *   O      [B, N, Hq, d]  fp32 output
- * d must be 128; Hq must be a multiple of Hkv.  All pointers 16-byte aligned.
- * ws: at least tr_verify_attn_workspace_bytes(...) bytes, zeroed once before
- * first use; every call leaves its counters at zero again. */
+ * d must be 128; Hq must be a multiple of Hkv; scale positive and finite.
+ * All pointers 16-byte aligned.  Keys are read in tiles of 64 positions:
+ * the cache rows from L[b] up to the next multiple of 64 (inside the buffer)
+ * are read and given weight zero, so they must hold finite values (a
+ * zero-initialised cache does).
+ * ws: at least tr_verify_attn_workspace_bytes(...) bytes of scratch (no
+ * initialisation needed); TR_E_INVAL for a bad argument, TR_E_UNSUPPORTED for
+ * d != 128, B > 1024 or sizes past the kernel's 31-bit tile indexing. */
 int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, const void *Kc, const void *Vc,
                    const int32_t *L, int cap, int B, int Hq, int Hkv, int d, float scale,
                    const struct tr_tree *tree, float *O, void *ws, size_t ws_bytes, tr_stream_t stream);

@@ -76,6 +76,9 @@ def test_host_validation_before_any_launch(lib):
                               None) == tr.TR_E_INVAL                                               # Hq % Hkv
     assert lib.tr_verify_attn(p, p, p, p, p, p, 64, 1, 4, 4, 64, 0.1, t.handle, p, p, 1 << 30,
                               None) == tr.TR_E_UNSUPPORTED                                         # d != 128
+    for bad_scale in (0.0, -0.1, float("inf"), float("nan")):
+        assert lib.tr_verify_attn(p, p, p, p, p, p, 64, 1, 4, 4, 128, bad_scale, t.handle, p, p, 1 << 30,
+                                  None) == tr.TR_E_INVAL                                           # scale
     assert lib.tr_update(p, tr.TR_I64, 1, 100, 8, t.handle, p, p, tr.TR_UPD_ACCEPTED, None, None,
                          None) == tr.TR_E_INVAL
     assert lib.tr_get_status(None, None) == tr.TR_E_INVAL
