@@ -10,9 +10,9 @@
 // ceil(N/64) tree tiles.  All pairs' tiles form one sequence that is cut into
 // equal contiguous ranges, one per CTA (one CTA per SM), so every SM streams
 // the same number of K/V bytes whatever the mix of prefix lengths.  A pair
-// that lies inside one range is finished in place; a pair cut by a range
-// boundary leaves (m, l, O) partials in two slots per CTA, and a small second
-// kernel merges them.
+// that lies inside one range is finished in place; a pair cut by range
+// boundaries leaves an (m, l, O) partial per part (two slots per CTA), and the
+// part that finishes last merges them.
 //
 // Per CTA (12 warps, so each SM sub-partition hosts one helper warp and two
 // softmax warps):
@@ -60,15 +60,17 @@ constexpr int kMaxB = 1024;
 
 template <int MT>
 struct Cfg {
-  static constexpr int KS = 4;                    // K ring stages
-  static constexpr int VS = MT == 1 ? 6 : 5;      // V ring stages
+  static constexpr int QB = MT == 1 ? 2 : 1;      // Q buffers (MT == 2: one, prefetched into L2)
+  static constexpr int KS = MT == 1 ? 3 : 4;      // K ring stages
+  static constexpr int VS = 5;                    // V ring stages
   static constexpr int GROUPS = MT == 1 ? 2 : 1;  // softmax warpgroups sharing one query head
   static constexpr int NSB = 4 / MT;              // S/P buffers in TMEM
   static constexpr int Q_HALF = 128 * 128;        // 128 rows x 64 bf16 (one d-half), bytes
   static constexpr int KV_HALF = 64 * 128;        // 64 keys x 64 bf16
   static constexpr int KV_TILE = 2 * KV_HALF;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + MT * 2 * Q_HALF;
+  static constexpr int Q_BUF = MT * 2 * Q_HALF;
+  static constexpr int OFF_K = OFF_Q + QB * Q_BUF;
   static constexpr int OFF_V = OFF_K + KS * KV_TILE;
   static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
   static constexpr int SOFT = 256;                // softmax threads: two warpgroups
@@ -82,13 +84,14 @@ static_assert(Cfg<2>::s_col(Cfg<2>::NSB - 1, 1) + BN <= Cfg<2>::TMEM_COLS, "TMEM
 
 template <int MT>
 struct Bars {
-  static constexpr int KS = Cfg<MT>::KS, VS = Cfg<MT>::VS, NSB = Cfg<MT>::NSB;
-  uint64_t q_full, q_empty;
+  static constexpr int QB = Cfg<MT>::QB, KS = Cfg<MT>::KS, VS = Cfg<MT>::VS, NSB = Cfg<MT>::NSB;
+  uint64_t q_full[QB], q_empty[QB];
   uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
   uint64_t s_full[NSB], p_full[NSB], pv_done[NSB];
   uint64_t o_full, o_empty, drain, ml_ready;
+  uint64_t mrg_in, mrg_go;  // hand-off of a pair shared by several CTAs
   uint32_t tmem;
-  int abort;
+  int abort, mrg_last;
   float2 ml_x[2][2][128];  // each warpgroup's (m, l) per row, by segment parity (MT == 1)
   int Ls[kMaxB];
   int pref[kMaxB + 1];  // first tile of sequence b in the global tile order
@@ -99,6 +102,7 @@ struct AttnArgs {
   float *O;
   float *part_o;      // [grid, 2, MT, N, d]
   float2 *part_ml;    // [grid, 2, MT, N]
+  int *cnt;           // [pairs] parts finished, back to zero after the merge
   unsigned *status;
   int B, N, Hq, Hkv, G, HG, cap;
   int q_rows, c_rows, t_rows;  // TMA box heights (at most the tensor's extent)
@@ -183,8 +187,10 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   const int N = a.N;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_empty, 1);
+    for (int q = 0; q < C::QB; ++q) {
+      mbar_init(&bars->q_full[q], 1);
+      mbar_init(&bars->q_empty[q], 1);
+    }
     for (int s = 0; s < KS; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -202,6 +208,8 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     mbar_init(&bars->o_empty, C::SOFT);
     mbar_init(&bars->drain, 2);  // one commit from each MMA issuer
     mbar_init(&bars->ml_ready, 256);
+    mbar_init(&bars->mrg_in, C::SOFT);
+    mbar_init(&bars->mrg_go, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -259,32 +267,18 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       const CUtensorMap *mt = is_k ? &tmKt : &tmVt;
       uint8_t *ring = smem + (is_k ? C::OFF_K : C::OFF_V);
       if (is_k) {
-        tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmKc);
         tma_prefetch_desc(&tmKt);
       } else {
         tma_prefetch_desc(&tmVc);
         tma_prefetch_desc(&tmVt);
       }
-      int cnt = 0, sc = 0, q_armed = -1, last[SMAX];
+      int cnt = 0, last[SMAX];
       for (int s = 0; s < SMAX; ++s) last[s] = -1;
       bool ok = true;
-      for (long long t = t_lo; t < t_hi && ok && !*abort; ++sc) {
+      for (long long t = t_lo; t < t_hi && ok && !*abort;) {
         const Seg sg = decode(t, t_lo, t_hi, bars->pref, bars->Ls, a);
         t += sg.n;
-        if (is_k) {
-          if (!mbar_wait(&bars->q_empty, (sc & 1) ^ 1, abort)) {
-            give_up();
-            break;
-          }
-          mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(MT * 2 * a.q_rows * 128));
-          for (int m = 0; m < MT; ++m) {
-            const int h = sg.g * a.G + sg.hg * MT + m;
-            for (int half = 0; half < 2; ++half)
-              tma_load_3d(smem + C::OFF_Q + (m * 2 + half) * C::Q_HALF, &tmQ, &bars->q_full, half * 64, h, sg.b * N);
-          }
-          q_armed = sc & 1;
-        }
         for (int u = 0; u < sg.n; ++u) {
           const int j = sg.j0 + u;
           const bool cache = j < sg.n_ct;
@@ -309,7 +303,6 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       }
       if (*abort) {
         // let the copies already issued land before the CTA can exit
-        if (q_armed >= 0) mbar_drain(&bars->q_full, (uint32_t)q_armed);
         for (int s = 0; s < NS; ++s)
           if (last[s] >= 0) mbar_drain(&full[s], (uint32_t)last[s]);
       }
@@ -319,15 +312,54 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     // S = Q.K^T of tile i once its Q and K have landed and the S/P buffer's
     // previous PV product has completed.  The whole warp runs the loop, so its
     // control flow and operands stay warp-uniform; one elected lane issues.
+    // This warp also loads Q: with two buffers the next segment's Q is loaded
+    // while the current one runs; with one, the next Q is prefetched into L2.
+    constexpr int QB = C::QB;
     constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
     const uint64_t dq0 = desc_kmajor_sw128(smem_u32(smem + C::OFF_Q));
     const uint64_t dk0 = desc_kmajor_sw128(smem_u32(smem + C::OFF_K));
+    int q_armed[QB];  // parity of the last Q load into each buffer, -1 for none
+    for (int q = 0; q < QB; ++q) q_armed[q] = -1;
+    auto load_q = [&](const Seg &sg, int sc_of) {
+      const int buf = sc_of % QB;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&bars->q_full[buf], (uint32_t)(MT * 2 * a.q_rows * 128));
+        for (int m = 0; m < MT; ++m) {
+          const int h = sg.g * a.G + sg.hg * MT + m;
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(smem + C::OFF_Q + buf * C::Q_BUF + (m * 2 + half) * C::Q_HALF, &tmQ, &bars->q_full[buf],
+                        half * 64, h, sg.b * N);
+        }
+      }
+      __syncwarp();
+      q_armed[buf] = (sc_of / QB) & 1;
+    };
     Cursor cq;
     cq.init(t_lo, t_hi, bars->pref, bars->Ls, a);
     const int n_all = (int)(t_hi - t_lo);
+    if (lane == 0) tma_prefetch_desc(&tmQ);
+    if (n_all > 0) {
+      load_q(cq.sg, 0);
+      if (QB == 2 && cq.t + cq.sg.n < t_hi) load_q(decode(cq.t + cq.sg.n, t_lo, t_hi, bars->pref, bars->Ls, a), 1);
+    }
     for (int i = 0; i < n_all; ++i) {
       const int sb = i % NSB, ks = i % KS;
-      if (cq.u == 0 && !wwait(&bars->q_full, cq.sc & 1)) break;
+      const int qb = cq.sc % QB;
+      if (cq.u == 0) {
+        const long long t_next = cq.t + cq.sg.n;  // first tile of the next segment
+        if (QB == 1 && cq.sc > 0) {
+          // the only buffer held the previous segment's Q: refill it once its last product is done
+          if (!wwait(&bars->q_empty[0], (cq.sc - 1) & 1)) break;
+          load_q(cq.sg, cq.sc);
+        }
+        if (QB == 1 && t_next < t_hi && lane == 0) {
+          const Seg nx = decode(t_next, t_lo, t_hi, bars->pref, bars->Ls, a);
+          for (int m = 0; m < MT; ++m)
+            for (int half = 0; half < 2; ++half)
+              tma_prefetch_l2_3d(&tmQ, half * 64, nx.g * a.G + nx.hg * MT + m, nx.b * N);
+        }
+        if (!wwait(&bars->q_full[qb], (cq.sc / QB) & 1)) break;
+      }
       if (!wwait(&bars->k_full[ks], (i / KS) & 1)) break;
       if (i >= NSB && !wwait(&bars->pv_done[sb], ((i / NSB) - 1) & 1)) break;
       tc_fence_after();
@@ -336,7 +368,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         const uint64_t dk = dk0 + (uint64_t)(ks * (C::KV_TILE >> 4));
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          const uint64_t dq = dq0 + (uint64_t)(m * (2 * C::Q_HALF >> 4));
+          const uint64_t dq = dq0 + (uint64_t)((qb * C::Q_BUF + m * 2 * C::Q_HALF) >> 4);
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k)
             mma_bf16(tmem + C::s_col(sb, m), dq + (uint64_t)(((k >> 2) * C::Q_HALF + (k & 3) * 32) >> 4),
@@ -344,10 +376,24 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         }
         mma_commit(&bars->k_empty[ks]);
         mma_commit(&bars->s_full[sb]);
-        if (cq.last()) mma_commit(&bars->q_empty);
+        if (cq.last()) mma_commit(&bars->q_empty[qb]);
       }
       __syncwarp();
+      if (QB == 2 && cq.u == 0 && cq.sc > 0) {
+        // after the segment's first product: the previous segment's buffer
+        // takes the next segment's Q once its last product is done
+        const long long t_next = cq.t + cq.sg.n;
+        if (t_next < t_hi) {
+          if (!wwait(&bars->q_empty[qb ^ 1], ((cq.sc - 1) / QB) & 1)) break;
+          load_q(decode(t_next, t_lo, t_hi, bars->pref, bars->Ls, a), cq.sc + 1);
+        }
+      }
       cq.advance(t_lo, t_hi, bars->pref, bars->Ls, a);
+    }
+    if (*abort) {
+      // let the Q copies already issued land before the CTA can exit
+      for (int q = 0; q < QB; ++q)
+        if (q_armed[q] >= 0) mbar_drain(&bars->q_full[q], (uint32_t)q_armed[q]);
     }
     if (elect_one()) mma_commit(&bars->drain);
     __syncwarp();
@@ -405,7 +451,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     const int rn = row_valid ? r : 0;
     const unsigned long long anc0 = tree.anc[rn][0], anc1 = tree.anc[rn][1];
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    int gt = 0, sc = 0;
+    int gt = 0, sc = 0, n_split = 0;
     bool ok = true;
     for (long long t = t_lo; t < t_hi && ok; ++sc) {
       const Seg sg = decode(t, t_lo, t_hi, bars->pref, bars->Ls, a);
@@ -565,6 +611,76 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&bars->o_empty);
       }
+      if (!sg.complete) {
+        // A pair shared by several CTAs (cut by range boundaries): each part
+        // leaves its partial in a slot and counts itself; the last part to
+        // finish merges them all and resets the counter.
+        const long long total = bars->pref[a.B];
+        const int grid = (int)gridDim.x;
+        const int tpp = tiles_per_pair(sg.Lb, N);
+        const long long first = bars->pref[sg.b] + (long long)(sg.g * a.HG + sg.hg) * tpp, last = first + tpp - 1;
+        // CTA c owns [total*c/grid, total*(c+1)/grid): the owner of tile t is ceil((t+1)*grid/total) - 1
+        const int c0 = (int)(((first + 1) * grid + total - 1) / total - 1);
+        const int c1 = (int)(((last + 1) * grid + total - 1) / total - 1);
+        __threadfence();
+        mbar_arrive(&bars->mrg_in);
+        if (threadIdx.x == 128) {
+          int is_last = 0;
+          if (mbar_wait(&bars->mrg_in, n_split & 1, abort)) {
+            __threadfence();
+            is_last = atomicAdd(&a.cnt[sg.pair], 1) == c1 - c0;
+            __threadfence();
+          } else {
+            give_up();
+          }
+          bars->mrg_last = is_last;
+          mbar_arrive(&bars->mrg_go);
+        }
+        if (!wwait(&bars->mrg_go, n_split & 1)) break;
+        ++n_split;
+        if (bars->mrg_last) {
+          __threadfence();
+          const int slot_c0 = c0 * 2 + (range_start(total, c0, grid) < first ? 1 : 0);
+          if (warp_active && row_valid) {
+#pragma unroll 1
+            for (int ch = col0; ch < col0 + COLS; ch += 64) {
+              float Mx = -INFINITY;
+#pragma unroll 1
+              for (int c = c0; c <= c1; ++c) {
+                const int slot = c == c0 ? slot_c0 : c * 2;
+                Mx = fmaxf(Mx, a.part_ml[((long long)slot * MT + mt) * N + r].x);
+              }
+              float acc[64];
+#pragma unroll
+              for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+              float den = 0.f;
+#pragma unroll 1
+              for (int c = c0; c <= c1; ++c) {
+                const int slot = c == c0 ? slot_c0 : c * 2;
+                const long long row = ((long long)slot * MT + mt) * N + r;
+                const float2 ml = a.part_ml[row];
+                const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - Mx);
+                den += ml.y * w;
+                const float4 *src = reinterpret_cast<const float4 *>(a.part_o + row * kD + ch);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float4 v = src[i];
+                  acc[4 * i] += v.x * w;
+                  acc[4 * i + 1] += v.y * w;
+                  acc[4 * i + 2] += v.z * w;
+                  acc[4 * i + 3] += v.w * w;
+                }
+              }
+              const float inv = 1.f / den;  // > 0: every node sees itself
+              float4 *dst = reinterpret_cast<float4 *>(a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD + ch);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                dst[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
+            }
+          }
+          if (threadIdx.x == 128) a.cnt[sg.pair] = 0;
+        }
+      }
       gt += T;
     }
   }
@@ -576,68 +692,6 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   }
 }
 
-// Merges the partials of every pair that two or more CTAs shared.  One block
-// per (pair, query head of the group), one thread per tree node.
-__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnArgs a, int MT, int grid) {
-  __shared__ int pref_s[kMaxB + 1];
-  __shared__ int Ls[kMaxB];
-  const int pair = blockIdx.x, m = blockIdx.y;
-  for (int b = threadIdx.x; b < a.B; b += blockDim.x) Ls[b] = min(max(a.L[b], 0), a.cap);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int b = 0; b < a.B; ++b) {
-      pref_s[b] = acc;
-      acc += tiles_per_pair(Ls[b], a.N) * a.Hkv * a.HG;
-    }
-    pref_s[a.B] = acc;
-  }
-  __syncthreads();
-  const int b = pair / (a.Hkv * a.HG), pib = pair % (a.Hkv * a.HG);
-  const int g = pib / a.HG, hg = pib % a.HG;
-  const long long total = pref_s[a.B];
-  const int tpp = tiles_per_pair(Ls[b], a.N);
-  const long long first = pref_s[b] + (long long)pib * tpp, last = first + tpp - 1;
-  // CTA c owns [total*c/grid, total*(c+1)/grid): the owner of tile t is ceil((t+1)*grid/total) - 1
-  const int c0 = (int)(((first + 1) * grid + total - 1) / total - 1);
-  const int c1 = (int)(((last + 1) * grid + total - 1) / total - 1);
-  if (c0 == c1) return;  // finished in place
-  const int n = threadIdx.x;
-  if (n >= a.N) return;
-  const int slot0 = c0 * 2 + (range_start(total, c0, grid) < first ? 1 : 0);
-  float M = -INFINITY;
-  for (int c = c0; c <= c1; ++c) {
-    const int slot = c == c0 ? slot0 : c * 2;
-    M = fmaxf(M, a.part_ml[((long long)slot * MT + m) * a.N + n].x);
-  }
-  float acc[kD];
-#pragma unroll
-  for (int i = 0; i < kD; ++i) acc[i] = 0.f;
-  float den = 0.f;
-  for (int c = c0; c <= c1; ++c) {
-    const int slot = c == c0 ? slot0 : c * 2;
-    const long long row = ((long long)slot * MT + m) * a.N + n;
-    const float2 ml = a.part_ml[row];
-    const float w = ml.x == -INFINITY ? 0.f : sm100::ex2(ml.x - M);
-    den += ml.y * w;
-    const float4 *src = reinterpret_cast<const float4 *>(a.part_o + row * kD);
-#pragma unroll
-    for (int i = 0; i < kD / 4; ++i) {
-      const float4 v = src[i];
-      acc[4 * i] += v.x * w;
-      acc[4 * i + 1] += v.y * w;
-      acc[4 * i + 2] += v.z * w;
-      acc[4 * i + 3] += v.w * w;
-    }
-  }
-  const float inv = 1.f / den;
-  const int h = g * a.G + hg * MT + m;
-  float4 *dst = reinterpret_cast<float4 *>(a.O + (((long long)b * a.N + n) * a.Hq + h) * kD);
-#pragma unroll
-  for (int i = 0; i < kD / 4; ++i)
-    dst[i] = make_float4(acc[4 * i] * inv, acc[4 * i + 1] * inv, acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
-}
-
 template <int MT>
 size_t smem_bytes() {
   return (size_t)Cfg<MT>::OFF_BAR + sizeof(Bars<MT>) + 1024;
@@ -645,7 +699,7 @@ size_t smem_bytes() {
 
 struct Plan {
   int G, MT, HG, pairs, grid;
-  size_t o_off, ml_off, total;
+  size_t o_off, ml_off, cnt_off, total;
 };
 
 Plan make_plan(int B, int Hq, int Hkv, int N) {
@@ -658,7 +712,8 @@ Plan make_plan(int B, int Hq, int Hkv, int N) {
   const size_t rows = (size_t)p.grid * 2 * p.MT * N;
   p.o_off = 0;
   p.ml_off = tr_align_up(rows * kD * sizeof(float), 256);
-  p.total = p.ml_off + tr_align_up(rows * sizeof(float2), 256);
+  p.cnt_off = p.ml_off + tr_align_up(rows * sizeof(float2), 256);
+  p.total = p.cnt_off + tr_align_up((size_t)p.pairs * sizeof(int), 256);
   return p;
 }
 
@@ -711,6 +766,7 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
   a.O = O;
   a.part_o = (float *)((char *)ws + p.o_off);
   a.part_ml = (float2 *)((char *)ws + p.ml_off);
+  a.cnt = (int *)((char *)ws + p.cnt_off);
   a.status = tr_status_dev();
   a.B = B;
   a.N = N;
@@ -742,8 +798,6 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
     }
     attn_tc_kernel<2><<<p.grid, Cfg<2>::THREADS, smem_bytes<2>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
   }
-  TR_LAUNCH_CHECK();
-  attn_merge_kernel<<<dim3(p.pairs, p.MT), 128, 0, s>>>(a, p.MT, p.grid);
   TR_LAUNCH_CHECK();
   return TR_OK;
 }

@@ -153,9 +153,10 @@ int tr_retrieve(const void *M, tr_itype mtype, int B, int64_t V, int K, const st
  * the cache rows from L[b] up to the next multiple of 64 (inside the buffer)
  * are read and given weight zero, so they must hold finite values (a
  * zero-initialised cache does).
- * ws: at least tr_verify_attn_workspace_bytes(...) bytes of scratch (no
- * initialisation needed); TR_E_INVAL for a bad argument, TR_E_UNSUPPORTED for
- * d != 128, B > 1024 or sizes past the kernel's 31-bit tile indexing. */
+ * ws: at least tr_verify_attn_workspace_bytes(...) bytes, zeroed once before
+ * first use; every call leaves its counters at zero again.  TR_E_INVAL for a
+ * bad argument, TR_E_UNSUPPORTED for d != 128, B > 1024 or sizes past the
+ * kernel's 31-bit tile indexing. */
 int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, const void *Kc, const void *Vc,
                    const int32_t *L, int cap, int B, int Hq, int Hkv, int d, float scale,
                    const struct tr_tree *tree, float *O, void *ws, size_t ws_bytes, tr_stream_t stream);
