@@ -1,37 +1,43 @@
 // Per-row top-K over vocabulary logits (fp32 or bf16), ties to the lower ID.
 //
 // The kernel streams each row once from HBM with 16-byte loads.  A row is cut
-// into `splits` chunks of about 8K elements so that the grid holds several
-// waves of short CTAs on 152 SMs whatever the row count.  Each thread keeps a
-// sorted register list of 64-bit keys (order-preserving value code in the
-// high word, complemented ID in the low word, so larger key = better and equal
-// values prefer the lower ID); a warp-wide floor computed from the lanes'
-// maxima rejects all but about 1% of the elements with one compare.  Lists merge by warp shuffles, then across warps, then across
-// the row's chunks in the last CTA to finish (an arrival counter in the
-// workspace, no spin-wait).
+// into `splits` chunks of at most 64 KB (16K fp32 or 32K bf16 elements), one
+// CTA each, and a chunk sits in registers (64 KB over 256 threads).  Keys are
+// 64-bit: an order-preserving value code in the high word and the
+// complemented ID in the low word, so a larger key is better and equal values
+// prefer the lower ID.  A floor taken from the lanes' maxima rejects all but
+// a fraction of a percent of the elements; the rest are counted, given slots
+// by a block-wide scan and ranked directly in shared memory.  The chunks of a
+// row form one thread-block cluster (up to 8: V up to 131072 fp32 or 262144
+// bf16) and merge through the first CTA's shared memory; longer rows merge in
+// the last CTA to finish (an arrival counter in the workspace, no spin-wait).
 #include "tr_internal.cuh"
 #include "tr_lists.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWindow = 16384;            // elements a CTA holds in registers (its whole chunk)
-constexpr long long kChunk = kWindow;     // target elements per CTA
+constexpr int kWindowBytes = 65536;      // bytes of a chunk a CTA holds in registers (64 a thread)
+constexpr long long kChunkF32 = kWindowBytes / 4;  // elements per chunk of fp32 rows (the most splits)
 constexpr int kRankKeys = 1024;           // keys ranked directly (also all chunks' lists of a row)
 constexpr int kMaxSplits = 32;
+constexpr int kMaxCluster = 8;  // portable thread-block cluster size
 
-// K-th largest of the lanes' values (counting repeats), the same on every lane.
+// K-th largest of the lanes' values (counting repeats), the same on every
+// lane: a bitonic sort of the 32 values into descending lane order.
 __device__ __forceinline__ float warp_kth(float v, int K, int lane) {
-  float res = -INFINITY;
-  for (int r = 0; r < K; ++r) {
-    float m = v;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    res = m;
-    const unsigned who = __ballot_sync(0xffffffffu, v == m);
-    if (lane == __ffs(who) - 1) v = -INFINITY;
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, j);
+      // blocks of k lanes alternate direction; the lower lane of a pair keeps
+      // the larger value in a descending block
+      const bool keep_max = ((lane & j) == 0) != ((lane & k) != 0);
+      v = keep_max ? fmaxf(v, o) : fminf(v, o);
+    }
   }
-  return res;
+  return __shfl_sync(0xffffffffu, v, K - 1);
 }
 
 template <typename T>
@@ -39,6 +45,7 @@ struct Elem;
 template <>
 struct Elem<float> {
   static constexpr int kVec = 4;
+  static constexpr bool kPrefilter = false;  // four compares cost less than a vector maximum
   template <int KMAX>
   __device__ __forceinline__ static void push_vec(TopList<KMAX> &L, const uint4 &q, uint32_t id) {
     L.push(__uint_as_float(q.x), id);
@@ -62,6 +69,7 @@ struct Elem<float> {
 template <>
 struct Elem<__nv_bfloat16> {
   static constexpr int kVec = 8;
+  static constexpr bool kPrefilter = true;   // packed maxima skip most unpacking
   template <int KMAX>
   __device__ __forceinline__ static void push_vec(TopList<KMAX> &L, const uint4 &q, uint32_t id) {
     L.push(__uint_as_float(q.x << 16), id);
@@ -85,11 +93,14 @@ struct Elem<__nv_bfloat16> {
     e[7] = __uint_as_float(q.w & 0xFFFF0000u);
   }
   __device__ __forceinline__ static float vmax(const uint4 &q) {
-    const float a = fmaxf(fmaxf(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xFFFF0000u)),
-                          fmaxf(__uint_as_float(q.y << 16), __uint_as_float(q.y & 0xFFFF0000u)));
-    const float b = fmaxf(fmaxf(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xFFFF0000u)),
-                          fmaxf(__uint_as_float(q.w << 16), __uint_as_float(q.w & 0xFFFF0000u)));
-    return fmaxf(a, b);
+    // packed maxima first (exact: a maximum needs no rounding)
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&q.x),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&q.y));
+    const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&q.z),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&q.w));
+    const __nv_bfloat162 c = __hmax2(a, b);
+    const uint32_t u = *reinterpret_cast<const uint32_t *>(&c);
+    return fmaxf(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
   }
   __device__ __forceinline__ static float load_again(const __nv_bfloat16 *p) {
     return __uint_as_float((uint32_t)__ldcg((const unsigned short *)p) << 16);
@@ -108,39 +119,62 @@ __device__ __forceinline__ void rank_select(const unsigned long long *keys, int 
   for (int k = threadIdx.x; k < n; k += blockDim.x) {
     const unsigned long long key = keys[k];
     int rank = 0;
+#pragma unroll 8
     for (int j = 0; j < n; ++j) rank += keys[j] > key;
     if (rank < K && key) out[rank] = key;
   }
   __syncthreads();
 }
 
-template <typename T, int KMAX, bool VEC>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long long V, long long ld, int K,
+// Thread-block cluster helpers: the rank of this CTA in its cluster, a store
+// into another CTA's shared memory, and the cluster-wide barrier.
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_u64(void *local_addr, unsigned rank, unsigned long long v) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(local_addr);
+  unsigned remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// CLUSTER: the row's chunks form one thread-block cluster and merge through
+// the first CTA's shared memory; otherwise through the workspace, the row's
+// last CTA to finish merging (an arrival counter, no spin-wait).
+template <typename T, int KMAX, bool VEC, bool CLUSTER>
+__global__ void __launch_bounds__(kThreads, KMAX <= 8 ? 3 : 1) topk_kernel(const T *logits, long long V, long long ld, int K,
                                                         long long chunk, int32_t *ids, float *vals,
                                                         unsigned long long *part, unsigned *counters) {
-  __shared__ unsigned short cand_o[kWindow];          // candidate offsets within the chunk
-  __shared__ unsigned long long keys[kRankKeys];       // keys being ranked
+  __shared__ unsigned long long keys[kRankKeys];       // candidate keys being ranked
   __shared__ unsigned long long top[TR_MAX_K];
+  __shared__ unsigned long long gathered[kMaxCluster * TR_MAX_K];  // the cluster's lists (first CTA)
   __shared__ unsigned long long warp_keys[kThreads / 32][KMAX];
   __shared__ float wfloor[kThreads / 32];
-  __shared__ int count, is_last;
+  __shared__ int wcount[kThreads / 32];
+  __shared__ int is_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, splits = gridDim.x;
   const long long row = blockIdx.y;
   const T *x = logits + row * ld;
   const long long lo = split * chunk;
   const long long hi = min(V, lo + chunk);
-  if (tid == 0) count = 0;
 
   bool ranked = false;
   if (VEC) {
-    // The chunk sits in registers.  The K-th largest lane maximum of a warp is
-    // reached by at least K elements of that warp, so no element strictly
-    // below the largest such warp floor can be in the row's top K.  Elements
-    // at or above it (about 1% of random logits) are compacted into shared
-    // memory with one ballot per element position and ranked directly.
+    // The chunk sits in registers (64 bytes a thread).  The K-th largest
+    // lane maximum of a warp is reached by at least K elements of that warp,
+    // so no element strictly below the largest such warp floor can be in the
+    // row's top K.  The elements at or above it (well under 1% of random
+    // logits) are counted, given slots by a block-wide scan, and ranked.
     constexpr int kV = Elem<T>::kVec;
-    constexpr int NV = kWindow / (kThreads * kV);
+    constexpr int NV = kWindowBytes / (kThreads * 16);
     const uint4 *xv = reinterpret_cast<const uint4 *>(x + lo);
     const int nvec = (int)((hi - lo) / kV);
     uint4 buf[NV];
@@ -149,7 +183,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long lo
       const int i = u * kThreads + tid;
       buf[u] = i < nvec ? __ldcs(xv + i) : Elem<T>::nan_vec();  // NaN never passes a compare
     }
-    float lm = -INFINITY;
+    // the ragged end of the chunk (fewer than one vector): one element for some threads
+    const long long tail0 = lo + (long long)nvec * kV;
+    const bool has_tail = tail0 + tid < hi;
+    const float tail_v = has_tail ? Elem<T>::load1(x + tail0 + tid) : NAN;
+    float lm = has_tail ? tail_v : -INFINITY;
 #pragma unroll
     for (int u = 0; u < NV; ++u) lm = fmaxf(lm, Elem<T>::vmax(buf[u]));
     const float wk = warp_kth(lm, K, lane);
@@ -158,63 +196,57 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long lo
     float floor_v = wfloor[0];
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) floor_v = fmaxf(floor_v, wfloor[w]);
-    const unsigned lt_mask = (1u << lane) - 1u;
+    // count, then a block-wide exclusive scan of the counts
+    // (bf16: a vector whose maximum is below the floor is skipped whole)
+    int cnt = has_tail && tail_v >= floor_v;
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-      float e[kV];
-      Elem<T>::unpack(buf[u], e);
+      if (!Elem<T>::kPrefilter || Elem<T>::vmax(buf[u]) >= floor_v) {
+        float e[kV];
+        Elem<T>::unpack(buf[u], e);
 #pragma unroll
-      for (int q = 0; q < kV; ++q) {
-        const bool c = e[q] >= floor_v;
-        const unsigned bal = __ballot_sync(0xffffffffu, c);
-        if (bal) {
-          int base = 0;
-          if (lane == 0) base = atomicAdd(&count, __popc(bal));
-          base = __shfl_sync(0xffffffffu, base, 0);
-          if (c) cand_o[base + __popc(bal & lt_mask)] = (unsigned short)((u * kThreads + tid) * kV + q);
-        }
+        for (int q = 0; q < kV; ++q) cnt += e[q] >= floor_v;
       }
     }
-    // the ragged end of the chunk (fewer than one vector)
-    const long long tail0 = lo + (long long)nvec * kV;
-    if (tail0 + tid < hi) {
-      const float v = Elem<T>::load1(x + tail0 + tid);
-      if (v >= floor_v) cand_o[atomicAdd(&count, 1)] = (unsigned short)(tail0 + tid - lo);
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
     }
+    if (lane == 31) wcount[warp] = incl;
     __syncthreads();
-    const int n = count;
+    int base = incl - cnt, n = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const int c = wcount[w];
+      base += w < warp ? c : 0;
+      n += c;
+    }
     if (n <= kRankKeys) {
-      for (int k = tid; k < n; k += kThreads) {
-        const long long id = lo + cand_o[k];
-        keys[k] = tr_key(tr_ord(Elem<T>::load_again(x + id)), (uint32_t)id);
+      // keys straight from the registers
+      if (cnt) {
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+          if (!Elem<T>::kPrefilter || Elem<T>::vmax(buf[u]) >= floor_v) {
+            float e[kV];
+            Elem<T>::unpack(buf[u], e);
+#pragma unroll
+            for (int q = 0; q < kV; ++q)
+              if (e[q] >= floor_v) keys[base++] = tr_key(tr_ord(e[q]), (uint32_t)(lo + (u * kThreads + tid) * kV + q));
+          }
+        }
+        if (has_tail && tail_v >= floor_v) keys[base] = tr_key(tr_ord(tail_v), (uint32_t)(tail0 + tid));
       }
+      __syncthreads();
       rank_select(keys, n, K, top);
       ranked = true;
-    } else {
-      // many ties at the floor: fold the candidates through register lists
-      TopList<KMAX> L;
-      L.init();
-      for (int k = tid; k < n; k += kThreads) {
-        const long long id = lo + cand_o[k];
-        L.push(Elem<T>::load_again(x + id), (uint32_t)id);
-      }
-      unsigned long long mine = warp_merge<KMAX>(L, lane);
-      if (lane < KMAX) warp_keys[warp][lane] = mine;
-      __syncthreads();
-      if (warp == 0) {
-        L.init();
-        if (lane < kThreads / 32)
-#pragma unroll
-          for (int j = 0; j < KMAX; ++j) L.k[j] = warp_keys[lane][j];
-        mine = warp_merge<KMAX>(L, lane);
-        if (lane < K) top[lane] = mine;
-      }
-      __syncthreads();
-      ranked = true;
     }
+    // else: many elements tie at the floor; the plain scan below takes the chunk again
   }
   if (!ranked) {
-    // rows that are not 16-byte aligned: a plain scan through register lists
+    // rows that are not 16-byte aligned (or chunks with more than kRankKeys
+    // elements at the floor): a plain scan through register lists
     TopList<KMAX> L;
     L.init();
     for (long long i = lo + tid; i < hi; i += kThreads) L.push(Elem<T>::load1(x + i), (uint32_t)i);
@@ -232,7 +264,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long lo
     __syncthreads();
   }
 
-  if (splits > 1) {
+  if (CLUSTER) {
+    // every chunk's list into the first CTA's shared memory, then one ranking there
+    const unsigned cr = cluster_rank();
+    if (tid < K) st_cluster_u64(&gathered[cr * K + tid], 0, top[tid]);
+    cluster_sync();
+    if (cr != 0) return;
+    rank_select(gathered, splits * K, K, top);
+  } else if (splits > 1) {
     // publish this chunk's top K; the row's last CTA to arrive ranks all chunks' keys
     if (tid < K) part[(row * splits + split) * KMAX + tid] = top[tid];
     __threadfence();
@@ -253,17 +292,37 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const T *logits, long lo
   }
 }
 
+template <typename T, int KMAX, bool VEC, bool CLUSTER>
+cudaError_t launch_one(const void *logits, long long rows, long long V, long long ld, int K, int splits, long long chunk,
+                int32_t *ids, float *vals, unsigned long long *part, unsigned *counters, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(splits, (unsigned)rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (CLUSTER) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, topk_kernel<T, KMAX, VEC, CLUSTER>, (const T *)logits, V, ld, K, chunk, ids, vals,
+                            part, counters);
+}
+
 template <typename T, int KMAX>
-void launch(const void *logits, long long rows, long long V, long long ld, int K, int splits, long long chunk,
+cudaError_t launch(const void *logits, long long rows, long long V, long long ld, int K, int splits, long long chunk,
             bool vec, int32_t *ids, float *vals, void *ws, size_t part_bytes, cudaStream_t s) {
   unsigned long long *part = (unsigned long long *)ws;
   unsigned *counters = (unsigned *)((char *)ws + part_bytes);
-  dim3 grid(splits, (unsigned)rows);
+  const bool cluster = splits > 1 && splits <= kMaxCluster;
   if (vec)
-    topk_kernel<T, KMAX, true><<<grid, kThreads, 0, s>>>((const T *)logits, V, ld, K, chunk, ids, vals, part, counters);
-  else
-    topk_kernel<T, KMAX, false><<<grid, kThreads, 0, s>>>((const T *)logits, V, ld, K, chunk, ids, vals, part,
-                                                          counters);
+    return cluster ? launch_one<T, KMAX, true, true>(logits, rows, V, ld, K, splits, chunk, ids, vals, part, counters, s)
+                   : launch_one<T, KMAX, true, false>(logits, rows, V, ld, K, splits, chunk, ids, vals, part, counters, s);
+  return cluster ? launch_one<T, KMAX, false, true>(logits, rows, V, ld, K, splits, chunk, ids, vals, part, counters, s)
+                 : launch_one<T, KMAX, false, false>(logits, rows, V, ld, K, splits, chunk, ids, vals, part, counters, s);
 }
 
 long long plan_chunk(long long V, int splits) {
@@ -278,12 +337,19 @@ size_t part_bytes_for(long long rows, int splits, int K) {
 
 }  // namespace
 
-int tr_topk_plan_splits(int64_t rows, int64_t V) {
-  (void)rows;
-  long long s = (V + kChunk - 1) / kChunk;
+// Chunks per row for elements of esz bytes; the workspace is laid out for
+// fp32 (the most chunks), so it also fits bf16 rows.
+static int plan_splits(int64_t V, size_t esz) {
+  const long long per = kWindowBytes / (long long)esz;
+  long long s = (V + per - 1) / per;
   if (s < 1) s = 1;
   if (s > kMaxSplits) s = kMaxSplits;
   return (int)s;
+}
+
+int tr_topk_plan_splits(int64_t rows, int64_t V) {
+  (void)rows;
+  return plan_splits(V, 4);
 }
 
 extern "C" size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K) {
@@ -295,23 +361,23 @@ extern "C" size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K) {
 
 int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K, int32_t *ids,
                    float *vals, void *ws, size_t ws_bytes, cudaStream_t s) {
-  const int splits = tr_topk_plan_splits(rows, V);
-  const long long chunk = splits > 1 ? plan_chunk(V, splits) : V;
   const size_t esz = ftype == TR_F32 ? 4 : 2;
-  const bool vec = ((uintptr_t)logits % 16 == 0) && ((ld * (int64_t)esz) % 16 == 0) && chunk <= kWindow;
-  const size_t pb = part_bytes_for(rows, splits, K);
+  const int splits = plan_splits(V, esz);
+  const long long chunk = splits > 1 ? plan_chunk(V, splits) : V;
+  const bool vec = ((uintptr_t)logits % 16 == 0) && ((ld * (int64_t)esz) % 16 == 0) &&
+                   chunk <= kWindowBytes / (long long)esz;
+  // the partial lists are laid out for the fp32 chunk count (never fewer chunks)
+  const size_t pb = part_bytes_for(rows, tr_topk_plan_splits(rows, V), K);
   const int km = tr_kmax(K);
 #define TR_TOPK_CASE(T, KM) launch<T, KM>(logits, rows, V, ld, K, splits, chunk, vec, ids, vals, ws, pb, s)
-  if (ftype == TR_F32) {
-    if (km == 8) TR_TOPK_CASE(float, 8);
-    else if (km == 16) TR_TOPK_CASE(float, 16);
-    else TR_TOPK_CASE(float, 32);
-  } else {
-    if (km == 8) TR_TOPK_CASE(__nv_bfloat16, 8);
-    else if (km == 16) TR_TOPK_CASE(__nv_bfloat16, 16);
-    else TR_TOPK_CASE(__nv_bfloat16, 32);
-  }
+  cudaError_t e;
+  if (ftype == TR_F32)
+    e = km == 8 ? TR_TOPK_CASE(float, 8) : km == 16 ? TR_TOPK_CASE(float, 16) : TR_TOPK_CASE(float, 32);
+  else
+    e = km == 8 ? TR_TOPK_CASE(__nv_bfloat16, 8) : km == 16 ? TR_TOPK_CASE(__nv_bfloat16, 16)
+                : TR_TOPK_CASE(__nv_bfloat16, 32);
 #undef TR_TOPK_CASE
+  if (e != cudaSuccess) return TR_E_CUDA;
   TR_LAUNCH_CHECK();
   (void)ws_bytes;
   return TR_OK;
