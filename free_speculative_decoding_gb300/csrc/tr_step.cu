@@ -274,10 +274,14 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const uint4 *Kt, const
   }
 }
 
-// The fused end of a step for sequence b, split over gridDim.y CTAs that share
-// the KV commit.  Every CTA evaluates the (cheap) acceptance itself; CTA 0
-// writes the outputs and updates M; the last CTA to arrive advances the loop
-// state and retrieves the next tree from the updated matrix.
+// The fused end of a step for sequence b.  CTA 0 of the sequence evaluates
+// the acceptance, updates M and retrieves the next tree at once: a small
+// shared-memory table maps every token written this step to its last writer
+// (BFS order), which both resolves duplicate writes and lets the retrieval
+// take a rewritten row from the new top-K rows it already holds, so it never
+// waits for its own global writes.  CTAs 1..G copy the accepted K/V rows
+// (each evaluates the cheap acceptance itself); the last of them to finish
+// advances L (CTA 0 does when there is no KV cache).
 struct FinishArgs {
   void *M;
   long long V;
@@ -293,50 +297,134 @@ struct FinishArgs {
   unsigned *status;
 };
 
+constexpr int kHash = 2 * TR_MAX_NODES;  // open addressing, load factor <= 1/2
+
+__device__ __forceinline__ int hash_slot(int t) { return (int)(((unsigned)t * 2654435761u) >> 24) & (kHash - 1); }
+
+struct WriterTable {
+  int key[kHash];   // token, -1 when empty
+  int node[kHash];  // last writing node (largest BFS index) of that token
+  __device__ __forceinline__ void insert(int t, int n) {
+    for (int h = hash_slot(t);; h = (h + 1) & (kHash - 1)) {
+      const int prev = atomicCAS(&key[h], -1, t);
+      if (prev == -1 || prev == t) {
+        atomicMax(&node[h], n);
+        return;
+      }
+    }
+  }
+  __device__ __forceinline__ int find(int t) const {
+    for (int h = hash_slot(t);; h = (h + 1) & (kHash - 1)) {
+      const int k = key[h];
+      if (k == t) return node[h];
+      if (k == -1) return -1;
+    }
+  }
+};
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) finish_kernel(FinishArgs a, const __grid_constant__ TreeDev tree) {
   __shared__ AcceptSmem s;
-  __shared__ bool writer[TR_MAX_NODES];
-  const int b = blockIdx.x, part = blockIdx.y, G = gridDim.y;
-  const int N = tree.N;
-  const int32_t *ids_b = a.ids + (long long)b * N * a.K;
-  load_tree_state(tree, a.tree_tok + (long long)b * N, ids_b, a.K, s);
-  if (threadIdx.x == 0) s.L = a.L[b];
+  __shared__ WriterTable wt;
+  __shared__ int32_t ids_s[TR_MAX_NODES * TR_MAX_K];
+  __shared__ int next_tok[TR_MAX_NODES];
+  const int b = blockIdx.x, part = blockIdx.y, G = gridDim.y - 1;  // G commit CTAs
+  const int N = tree.N, K = a.K, n = threadIdx.x;
+  const int32_t *ids_b = a.ids + (long long)b * N * K;
+  if (part == 0) {
+    for (int h = n; h < kHash; h += blockDim.x) {
+      wt.key[h] = -1;
+      wt.node[h] = -1;
+    }
+  }
+  load_tree_state(tree, a.tree_tok + (long long)b * N, ids_b, K, s);
   block_accept(tree, s);
-  const int acc = s.acc_len, Lb = s.L;
-  T *Mb = (T *)a.M + (long long)b * a.V * a.K;
+  const int acc = s.acc_len;
   if (part == 0) {
     write_accept_outputs(tree, s, b, a.acc_len, a.path, a.committed, nullptr);
-    const int n = threadIdx.x;
-    if (n < N) writer[n] = a.mode == TR_UPD_ALL || ((tree.anc[s.best][n >> 6] >> (n & 63)) & 1ull);
+    T *Mb = (T *)a.M + (long long)b * a.V * K;
+    // writers: every node, or the accepted path; their top-K rows into shared memory
+    bool w = false;
+    int t = 0;
+    if (n < N) {
+      w = a.mode == TR_UPD_ALL || ((tree.anc[s.best][n >> 6] >> (n & 63)) & 1ull);
+      t = s.tok[n];
+      if (w && (t < 0 || (long long)t >= a.V)) {
+        tr_flag(a.status, TR_DEV_BAD_TOKEN);
+        w = false;
+      }
+      if (w) {
+        for (int k = 0; k < K; ++k) ids_s[n * K + k] = ids_b[(long long)n * K + k];
+        wt.insert(t, n);
+      }
+    }
     __syncthreads();
-    block_update<T>(Mb, a.V, a.K, tree, s.tok, writer, ids_b, a.status);
+    // last writer in BFS order stores its row
+    if (w && wt.find(t) == n) {
+      T *row = Mb + (long long)t * K;
+      for (int k = 0; k < K; ++k) row[k] = (T)ids_s[n * K + k];
+    }
+    // the next tree from the updated matrix: rows written this step come from ids_s
+    if (n < 32) {
+      const int lane = n;
+      if (lane == 0) {
+        int root = s.bonus;
+        if (root < 0 || (long long)root >= a.V) {
+          tr_flag(a.status, TR_DEV_BAD_TOKEN);
+          root = 0;
+        }
+        next_tok[0] = root;
+      }
+      __syncwarp();
+      for (int l = 1; l <= tree.D; ++l) {
+        const int lo = tree.level_off[l], hi = tree.level_off[l + 1];
+        for (int m = lo + lane; m < hi; m += 32) {
+          const int tp = next_tok[tree.parent[m]], r = tree.rank[m];
+          const int wr = wt.find(tp);
+          long long v = wr >= 0 ? (long long)ids_s[wr * K + r] : (long long)Mb[(long long)tp * K + r];
+          if (v < 0 || v >= a.V) {
+            tr_flag(a.status, TR_DEV_BAD_TOKEN);
+            v = 0;
+          }
+          next_tok[m] = (int)v;
+        }
+        __syncwarp();
+      }
+      int32_t *out = a.tree_tok + (long long)b * N;
+      for (int m = lane; m < N; m += 32) out[m] = next_tok[m];
+      if (lane == 0) {
+        a.root[b] = s.bonus;
+        if (G == 0) {
+          const int Lb = a.L[b];
+          if (Lb < 0 || Lb > a.cap) tr_flag(a.status, TR_DEV_BAD_LENGTH);
+          else if (a.Kc && Lb + acc + 1 > a.cap) tr_flag(a.status, TR_DEV_CACHE_FULL);
+          else a.L[b] = Lb + acc + 1;
+        }
+      }
+    }
+    return;
   }
+  // ---- KV commit of heads [h_lo, h_hi)
+  if (threadIdx.x == 0) s.L = a.L[b];
+  __syncthreads();
+  const int Lb = s.L;
   const bool bad_len = Lb < 0 || Lb > a.cap;
-  const bool full = !bad_len && a.Kc && Lb + acc + 1 > a.cap;
-  if (a.Kc && !bad_len && !full) {
-    const int h_lo = part * a.heads_per_cta, h_hi = min(a.Hkv, h_lo + a.heads_per_cta);
+  const bool full = !bad_len && Lb + acc + 1 > a.cap;
+  if (!bad_len && !full) {
+    const int h_lo = (part - 1) * a.heads_per_cta, h_hi = min(a.Hkv, h_lo + a.heads_per_cta);
     if (h_lo < h_hi) block_commit(a.Kt, a.Vt, a.Kc, a.Vc, N, a.Hkv, a.cap, a.d16, b, Lb, acc, s.path, h_lo, h_hi);
   }
-  __threadfence();
+  // the last commit CTA of the sequence advances L (every one has read it by then)
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned prev = G > 1 ? atomicAdd(&a.counters[b], 1u) : 0u;
-    s.last = prev == (unsigned)(G - 1);
+    const unsigned prev = G > 1 ? atomicAdd(&a.counters[b], 1u) : 0u;
+    if (prev == (unsigned)(G - 1)) {
+      if (bad_len) tr_flag(a.status, TR_DEV_BAD_LENGTH);
+      else if (full) tr_flag(a.status, TR_DEV_CACHE_FULL);
+      else a.L[b] = Lb + acc + 1;
+      if (G > 1) a.counters[b] = 0u;
+    }
   }
-  __syncthreads();
-  if (!s.last) return;
-  __threadfence();
-  if (threadIdx.x == 0) {
-    if (bad_len) tr_flag(a.status, TR_DEV_BAD_LENGTH);
-    else if (full) tr_flag(a.status, TR_DEV_CACHE_FULL);
-    else a.L[b] = Lb + acc + 1;
-    a.root[b] = s.bonus;
-    if (G > 1) a.counters[b] = 0u;
-  }
-  if (threadIdx.x < 32)
-    warp_retrieve<T>(Mb, a.V, a.K, tree, s.bonus, s.path /* reused as scratch */, a.tree_tok + (long long)b * N,
-                     a.status);
 }
 
 int commit_heads_per_cta(int Hkv) {
@@ -472,11 +560,11 @@ extern "C" int tr_step(const tr_step_args *a, tr_stream_t stream) {
   f.mode = a->mode;
   f.counters = (unsigned *)((char *)a->ws + tk_ws);
   f.status = tr_status_dev();
-  const int G = commit ? (a->Hkv + f.heads_per_cta - 1) / f.heads_per_cta : 1;
+  const int G = commit ? (a->Hkv + f.heads_per_cta - 1) / f.heads_per_cta : 0;  // commit CTAs per sequence
   if (a->mtype == TR_I64)
-    finish_kernel<long long><<<dim3(a->B, G), kThreads, 0, s>>>(f, tree);
+    finish_kernel<long long><<<dim3(a->B, 1 + G), kThreads, 0, s>>>(f, tree);
   else
-    finish_kernel<int32_t><<<dim3(a->B, G), kThreads, 0, s>>>(f, tree);
+    finish_kernel<int32_t><<<dim3(a->B, 1 + G), kThreads, 0, s>>>(f, tree);
   TR_LAUNCH_CHECK();
   return TR_OK;
 }
