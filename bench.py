@@ -39,9 +39,10 @@ import synth  # noqa: E402
 
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# dram bytes per launch of the dominant kernel from an ncu capture, valid only
-# while the kernel source is unchanged (sha256 of its .cu file)
-TRAFFIC = {}
+# dram bytes per launch of the dominant kernel from an ncu capture of this
+# workload (dram__bytes_read.sum + dram__bytes_write.sum, mean of two launches),
+# valid only while the kernel's sources are unchanged (sha256 of the files)
+TRAFFIC = {"attn": {"bytes": 653311616 + 19128320, "sha": "a78f9bc8e8020913", "files": ("tr_attn.cu", "tr_sm100.cuh")}}
 
 
 PRIME_CYCLES = 2_000_000   # about 1 ms of device time at the GB300's clocks
@@ -56,10 +57,12 @@ def load_peaks():
     return PEAK_FALLBACK, "fallback"
 
 
-def src_sha(name):
-    p = os.path.join(ROOT, "free_speculative_decoding_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_sha(*names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "free_speculative_decoding_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 # ----------------------------------------------------------------------------
@@ -483,7 +486,7 @@ def main():
         ach = a_bytes / (a_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
         tr_ = TRAFFIC.get("attn")
-        traffic = tr_["bytes"] if tr_ and tr_["sha"] == src_sha("tr_attn.cu") else None
+        traffic = tr_["bytes"] if tr_ and tr_["sha"] == src_sha(*tr_["files"]) and args.workload == "batched" else None
         roofline = {"kernel": "tr_verify_attn", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
                     "frac": ach / peak, "traffic": traffic, "peak_source": peak_kind,
                     "algorithmic_bytes_per_launch": a_bytes, "ms_per_launch": a_ms}
