@@ -5,9 +5,10 @@
 //   warp 0      TMA producer: 128x64 H and 256x64 Wt tiles, 128-byte swizzle,
 //               a 4-stage shared-memory ring guarded by mbarriers;
 //   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
-//               one thread issues tcgen05.mma (M=128, N=256, K=16) per 16-wide
-//               K slice, committing each stage back to the producer and each
-//               finished tile to the epilogue;
+//               issues tcgen05.mma (M=128, N=256, K=16) per 16-wide K slice,
+//               committing each stage back to the producer and each finished
+//               tile to the epilogue; the warp runs its loop warp-uniformly
+//               and one elected lane issues;
 //   warps 2..5  epilogue: each thread owns one TMEM lane (one hidden row) and
 //               streams the tile's 256 fp32 logits from TMEM into a register
 //               top-K list, then writes that list (one per row and tile).
@@ -107,42 +108,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      int it = 0, tc = 0;
-      for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x, ++tc) {
-        const int acc = tc & 1;
-        const uint32_t aph = (tc >> 1) & 1;
-        if (!mbar_wait(&bars->tempty[acc], aph ^ 1, abort)) {
-          give_up();
+    // The whole warp runs the loop, so control flow and operands stay
+    // warp-uniform; one elected lane issues the MMAs and commits.
+    auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
+      const bool all = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+      if (!all && lane == 0) give_up();
+      return all;
+    };
+    const uint64_t da0 = desc_kmajor_sw128(smem_u32(smem));
+    int it = 0, tc = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tc) {
+      const int acc = tc & 1;
+      const uint32_t aph = (tc >> 1) & 1;
+      if (!wwait(&bars->tempty[acc], aph ^ 1)) break;
+      tc_fence_after();
+      const uint32_t d = tmem + (uint32_t)(acc * BN);
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1;
+        if (!wwait(&bars->full[s], ph)) {
+          ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(acc * BN);
-        bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&bars->full[s], ph, abort)) {
-            give_up();
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
-          const uint32_t b0 = a0 + A_BYTES;
+        if (elect_one()) {
+          // descriptor start addresses count 16-byte units
+          const uint64_t da = da0 + (uint64_t)(s * (STAGE_BYTES >> 4));
+          const uint64_t db = da + (uint64_t)(A_BYTES >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(d, desc_kmajor_sw128(a0 + k * 32), desc_kmajor_sw128(b0 + k * 32), kIdesc,
-                     (kb | k) != 0 ? 1u : 0u);
+            mma_bf16(d, da + (uint64_t)(k * 2), db + (uint64_t)(k * 2), kIdesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit(&bars->empty[s]);
+          if (kb == nkb - 1) mma_commit(&bars->tfull[acc]);
         }
-        if (!ok) break;
-        mma_commit(&bars->tfull[acc]);
+        __syncwarp();
       }
-      // every MMA issued so far completes before TMEM can be released
-      mma_commit(&bars->drain);
-      mbar_drain(&bars->drain, 0);
+      if (!ok) break;
     }
+    // every MMA issued so far completes before TMEM can be released
+    if (elect_one()) mma_commit(&bars->drain);
+    __syncwarp();
+    mbar_drain(&bars->drain, 0);
   } else {
     const int lane_base = (warp & 3) * 32;  // TMEM lanes this warp may read
     int tc = 0;
