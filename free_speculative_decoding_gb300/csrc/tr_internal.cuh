@@ -84,6 +84,6 @@ static inline size_t tr_align_up(size_t x, size_t a) { return (x + a - 1) / a * 
 static inline int tr_kmax(int K) { return K <= 8 ? 8 : (K <= 16 ? 16 : 32); }
 
 // top-K internals shared with the step and the LM head
-int tr_topk_plan_splits(int64_t rows, int64_t V);
+size_t tr_topk_counters_offset(int64_t rows, int64_t V, int K);  // byte offset of the arrival counters in the workspace
 int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K,
                    int32_t *ids, float *vals, void *ws, size_t ws_bytes, cudaStream_t stream);

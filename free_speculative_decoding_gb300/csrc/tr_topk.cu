@@ -1,60 +1,42 @@
 // Per-row top-K over vocabulary logits (fp32 or bf16), ties to the lower ID.
 //
-// The kernel streams each row once from HBM with 16-byte loads.  A row is cut
-// into `splits` chunks of at most 64 KB (16K fp32 or 32K bf16 elements), one
-// CTA each, and a chunk sits in registers (64 KB over 256 threads).  Keys are
-// 64-bit: an order-preserving value code in the high word and the
+// Keys are 64-bit: an order-preserving value code in the high word and the
 // complemented ID in the low word, so a larger key is better and equal values
-// prefer the lower ID.  A floor taken from the lanes' maxima rejects all but
-// a fraction of a percent of the elements; the rest are counted, given slots
-// by a block-wide scan and ranked directly in shared memory.  The chunks of a
-// row form one thread-block cluster (up to 8: V up to 131072 fp32 or 262144
-// bf16) and merge through the first CTA's shared memory; longer rows merge in
-// the last CTA to finish (an arrival counter in the workspace, no spin-wait).
+// prefer the lower ID.
+//
+// Rows whose start and stride are 16-byte aligned take the warp-streaming
+// kernel.  Every row is cut into 8 KB steps; all rows' steps, in order, are
+// cut into equal contiguous ranges, one per warp of a persistent grid (one
+// CTA of 8 warps per SM).  Each warp pulls its steps through a private ring
+// of three bulk copies (cp.async.bulk into shared memory, completing on an
+// mbarrier), copies the step at hand into registers, and keeps the current
+// row's running top-K across its lanes (lane j holds the j-th best key).
+// Only elements above a floor can enter: the K-th best value held, or on a
+// segment's first step the K-th largest lane maximum.  A step with no lane
+// maximum above the floor costs a vector maximum and one vote; otherwise each
+// lane hands over its largest remaining element per pass and the warp inserts
+// those keys by ballot and shuffle.  A row split between warps leaves one
+// list per warp segment in the workspace; the warp that completes the row's
+// step count merges them.
+//
+// Other rows take a plain scan: a row is cut into chunks of one 256-thread
+// CTA each, every thread keeps a register list, and the chunks of a row merge
+// inside a thread-block cluster (or, beyond 8 chunks, in the last CTA to
+// finish).
 #include "tr_internal.cuh"
 #include "tr_lists.cuh"
+#include "tr_sm100.cuh"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWindowBytes = 65536;      // bytes of a chunk a CTA holds in registers (64 a thread)
-constexpr long long kChunkF32 = kWindowBytes / 4;  // elements per chunk of fp32 rows (the most splits)
-constexpr int kRankKeys = 1024;           // keys ranked directly (also all chunks' lists of a row)
-constexpr int kMaxSplits = 32;
-constexpr int kMaxCluster = 8;  // portable thread-block cluster size
-
-// K-th largest of the lanes' values (counting repeats), the same on every
-// lane: a bitonic sort of the 32 values into descending lane order.
-__device__ __forceinline__ float warp_kth(float v, int K, int lane) {
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, v, j);
-      // blocks of k lanes alternate direction; the lower lane of a pair keeps
-      // the larger value in a descending block
-      const bool keep_max = ((lane & j) == 0) != ((lane & k) != 0);
-      v = keep_max ? fmaxf(v, o) : fminf(v, o);
-    }
-  }
-  return __shfl_sync(0xffffffffu, v, K - 1);
-}
+constexpr unsigned kFull = 0xffffffffu;
 
 template <typename T>
 struct Elem;
 template <>
 struct Elem<float> {
   static constexpr int kVec = 4;
-  static constexpr bool kPrefilter = false;  // four compares cost less than a vector maximum
-  template <int KMAX>
-  __device__ __forceinline__ static void push_vec(TopList<KMAX> &L, const uint4 &q, uint32_t id) {
-    L.push(__uint_as_float(q.x), id);
-    L.push(__uint_as_float(q.y), id + 1);
-    L.push(__uint_as_float(q.z), id + 2);
-    L.push(__uint_as_float(q.w), id + 3);
-  }
   __device__ __forceinline__ static float load1(const float *p) { return __ldcs(p); }
-  __device__ __forceinline__ static float load_again(const float *p) { return __ldcg(p); }
   __device__ __forceinline__ static uint4 nan_vec() { return make_uint4(0x7FC00000u, 0x7FC00000u, 0x7FC00000u, 0x7FC00000u); }
   __device__ __forceinline__ static void unpack(const uint4 &q, float (&e)[4]) {
     e[0] = __uint_as_float(q.x);
@@ -62,6 +44,15 @@ struct Elem<float> {
     e[2] = __uint_as_float(q.z);
     e[3] = __uint_as_float(q.w);
   }
+  // the vector with component k set to NaN
+  __device__ __forceinline__ static uint4 clear(uint4 q, int k) {
+    q.x = k == 0 ? 0x7FC00000u : q.x;
+    q.y = k == 1 ? 0x7FC00000u : q.y;
+    q.z = k == 2 ? 0x7FC00000u : q.z;
+    q.w = k == 3 ? 0x7FC00000u : q.w;
+    return q;
+  }
+  // maximum of the vector, NaN only if all four are NaN
   __device__ __forceinline__ static float vmax(const uint4 &q) {
     return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)), fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
   }
@@ -69,18 +60,6 @@ struct Elem<float> {
 template <>
 struct Elem<__nv_bfloat16> {
   static constexpr int kVec = 8;
-  static constexpr bool kPrefilter = true;   // packed maxima skip most unpacking
-  template <int KMAX>
-  __device__ __forceinline__ static void push_vec(TopList<KMAX> &L, const uint4 &q, uint32_t id) {
-    L.push(__uint_as_float(q.x << 16), id);
-    L.push(__uint_as_float(q.x & 0xFFFF0000u), id + 1);
-    L.push(__uint_as_float(q.y << 16), id + 2);
-    L.push(__uint_as_float(q.y & 0xFFFF0000u), id + 3);
-    L.push(__uint_as_float(q.z << 16), id + 4);
-    L.push(__uint_as_float(q.z & 0xFFFF0000u), id + 5);
-    L.push(__uint_as_float(q.w << 16), id + 6);
-    L.push(__uint_as_float(q.w & 0xFFFF0000u), id + 7);
-  }
   __device__ __forceinline__ static uint4 nan_vec() { return make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u); }
   __device__ __forceinline__ static void unpack(const uint4 &q, float (&e)[8]) {
     e[0] = __uint_as_float(q.x << 16);
@@ -92,8 +71,19 @@ struct Elem<__nv_bfloat16> {
     e[6] = __uint_as_float(q.w << 16);
     e[7] = __uint_as_float(q.w & 0xFFFF0000u);
   }
+  // the vector with element k set to NaN (even k: low half of word k/2)
+  __device__ __forceinline__ static uint4 clear(uint4 q, int k) {
+    const uint32_t nan = (k & 1) ? 0x7FC00000u : 0x00007FC0u, keep = (k & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+    const int w = k >> 1;
+    q.x = w == 0 ? (q.x & keep) | nan : q.x;
+    q.y = w == 1 ? (q.y & keep) | nan : q.y;
+    q.z = w == 2 ? (q.z & keep) | nan : q.z;
+    q.w = w == 3 ? (q.w & keep) | nan : q.w;
+    return q;
+  }
   __device__ __forceinline__ static float vmax(const uint4 &q) {
-    // packed maxima first (exact: a maximum needs no rounding)
+    // packed maxima first (exact: a maximum needs no rounding; NaN is dropped
+    // unless both inputs are NaN)
     const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&q.x),
                                      *reinterpret_cast<const __nv_bfloat162 *>(&q.y));
     const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&q.z),
@@ -102,14 +92,297 @@ struct Elem<__nv_bfloat16> {
     const uint32_t u = *reinterpret_cast<const uint32_t *>(&c);
     return fmaxf(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
   }
-  __device__ __forceinline__ static float load_again(const __nv_bfloat16 *p) {
-    return __uint_as_float((uint32_t)__ldcg((const unsigned short *)p) << 16);
-  }
   __device__ __forceinline__ static float load1(const __nv_bfloat16 *p) {
     const unsigned short u = __ldcs((const unsigned short *)p);
     return __uint_as_float((uint32_t)u << 16);
   }
 };
+
+// ---------------------------------------------------------------------------
+// warp-streaming kernel (aligned rows)
+// ---------------------------------------------------------------------------
+
+constexpr int kVecs = 16;                // 16-byte vectors a lane loads per step
+constexpr int kStep = 32 * kVecs * 16;   // bytes of a row one warp step covers (8 KB)
+constexpr int kWarps = 8;                // warps per CTA (one CTA per SM)
+constexpr int kStages = 3;               // steps a warp has in flight or in hand
+
+struct alignas(128) WarpRing {
+  unsigned char stage[kStages][kStep];
+  uint64_t full[kStages];
+};
+constexpr size_t kRingSmem = sizeof(WarpRing) * kWarps + 128;  // +128: alignment of the base
+
+// steps per row for elements of esz bytes
+inline long long steps_per_row(long long V, size_t esz) { return (V * (long long)esz + kStep - 1) / kStep; }
+
+// The contiguous step range [u0, u1) of warp w out of W over U steps, and the
+// warp whose range holds step u.
+__device__ __forceinline__ long long range_start(long long w, long long U, long long W) { return w * U / W; }
+__device__ __forceinline__ long long warp_of(long long u, long long U, long long W) { return ((u + 1) * W - 1) / U; }
+
+// K-th largest of the lanes' values (counting repeats), the same on every
+// lane: a bitonic sort of the 32 values into descending lane order.
+__device__ __forceinline__ float warp_kth(float v, int K, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(kFull, v, j);
+      // blocks of k lanes alternate direction; the lower lane of a pair keeps
+      // the larger value in a descending block
+      const bool keep_max = ((lane & j) == 0) != ((lane & k) != 0);
+      v = keep_max ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  return __shfl_sync(kFull, v, K - 1);
+}
+
+__device__ __forceinline__ void write_final(int32_t *ids, float *vals, long long row, int K, int lane,
+                                            unsigned long long key) {
+  if (lane < K) {
+    ids[row * K + lane] = key ? (int32_t)tr_key_id(key) : -1;
+    if (vals) vals[row * K + lane] = key ? tr_key_val(key) : -INFINITY;
+  }
+}
+
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    topk_warp_kernel(const T *__restrict__ x, long long V, long long ld, int K, int nch, long long U, int32_t *ids,
+                     float *vals, unsigned long long *part, unsigned *counters, unsigned *status) {
+  using namespace sm100;
+  extern __shared__ unsigned char smem_raw[];
+  const int lane = threadIdx.x & 31;
+  WarpRing &ring = reinterpret_cast<WarpRing *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                                ~uintptr_t(127))[threadIdx.x >> 5];
+  const long long W = (long long)gridDim.x * kWarps;
+  const long long gw = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const long long u0 = range_start(gw, U, W), u1 = range_start(gw + 1, U, W);
+  if (u0 >= u1) return;  // warps work alone: no block-wide barrier follows
+
+  constexpr int kV = Elem<T>::kVec;
+  constexpr int kN = kVecs * kV;  // elements of a lane per step
+  const long long row_bytes = V * (long long)sizeof(T);
+  const int n_steps = (int)(u1 - u0);
+
+  // lane j < K: the j-th best key of the row segment so far
+  unsigned long long lk = 0ull;
+  bool have_k = false;  // K keys held: thr is the value of the K-th
+  float thr = 0.f;
+  long long cur = -1;   // row of the segment
+  int seg_first = 0, seg_units = 0;
+
+  // end of a row segment: the final list, or this segment's list for a merge
+  auto flush = [&](long long row) {
+    if (seg_first == 0 && seg_units == nch) {
+      write_final(ids, vals, row, K, lane, lk);
+      return;
+    }
+    if (lane < K) part[((unsigned long long)row * nch + seg_first) * KMAX + lane] = lk;
+    __threadfence();
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) last = atomicAdd(&counters[row], (unsigned)seg_units) + (unsigned)seg_units == (unsigned)nch;
+    if (!__shfl_sync(kFull, last, 0)) return;
+    __threadfence();
+    // every warp segment of the row left its list at the slot of its first step
+    TopList<KMAX> L;
+    L.init();
+    const long long r0 = row * nch;
+    const long long wlo = warp_of(r0, U, W), whi = warp_of(r0 + nch - 1, U, W);
+    for (long long p = wlo + lane; p <= whi; p += 32) {
+      const long long sp = range_start(p, U, W);
+      if (sp >= range_start(p + 1, U, W)) continue;  // a warp without steps
+      const long long first = (sp > r0 ? sp : r0) - r0;
+      const unsigned long long *src = part + ((unsigned long long)row * nch + first) * KMAX;
+      for (int j = 0; j < K; ++j) list_insert(L.k, __ldcg(src + j));
+    }
+    const unsigned long long m = warp_merge<KMAX>(L, lane);
+    write_final(ids, vals, row, K, lane, m);
+    if (lane == 0) counters[row] = 0u;  // the workspace is left zeroed
+  };
+
+  // A ring of kStages bulk copies (cp.async.bulk into this warp's shared
+  // memory) runs ahead of the step being examined.  Lane 0 issues the copy of
+  // the next step (row ir, step ic of the row): its whole 16-byte vectors;
+  // the row's ragged last bytes are read directly.
+  const char *base = reinterpret_cast<const char *>(x);
+  const long long stride = ld * (long long)sizeof(T);
+  long long ir = u0 / nch;
+  int ic = (int)(u0 - ir * nch), n_issued = 0;
+  if (lane == 0) {
+    for (int q = 0; q < kStages; ++q) mbar_init(&ring.full[q], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  auto issue = [&](int q) {
+    const long long off = (long long)ic * kStep;
+    const uint32_t bytes = (uint32_t)(min(row_bytes - off, (long long)kStep) & ~15ll);
+    mbar_arrive_expect_tx(&ring.full[q], bytes);
+    if (bytes) bulk_load(ring.stage[q], base + ir * stride + off, bytes, &ring.full[q]);
+    if (++ic == nch) {
+      ic = 0;
+      ++ir;
+    }
+    ++n_issued;
+  };
+  if (lane == 0)
+    for (int q = 0; q < kStages && q < n_steps; ++q) issue(q);
+
+  // stage q's step (row r, step c of the row) into v, NaN past the row's last
+  // whole vector; then the stage takes the next step to fetch
+  auto fetch = [&](uint4 (&v)[kVecs], int q, long long r, int c) {
+    const int nvec = (int)(min(row_bytes - (long long)c * kStep, (long long)kStep) >> 4);
+    const uint4 *sv = reinterpret_cast<const uint4 *>(ring.stage[q]);
+    if (nvec == 32 * kVecs) {
+#pragma unroll
+      for (int j = 0; j < kVecs; ++j) v[j] = sv[j * 32 + lane];
+    } else {
+#pragma unroll
+      for (int j = 0; j < kVecs; ++j) {
+        const int i = j * 32 + lane;
+        v[j] = i < nvec ? sv[i] : Elem<T>::nan_vec();  // NaN never passes a compare
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      fence_proxy_async_smem();  // the stage's reads come before the next copy into it
+      if (n_issued < n_steps) issue(q);
+    }
+  };
+
+  auto process = [&](uint4 (&v)[kVecs], long long r, int c) {
+    if (r != cur) {
+      if (cur >= 0) flush(cur);
+      cur = r;
+      lk = 0ull;
+      have_k = false;
+      seg_first = c;
+      seg_units = 0;
+    }
+    ++seg_units;
+    const long long off = (long long)c * kStep;
+    const long long nb = min(row_bytes - off, (long long)kStep);
+    const long long id0 = off / (long long)sizeof(T);                      // first element of the step
+    const long long et = id0 + (nb >> 4) * kV;                              // first element past the vectors
+    const int ntail = (int)((nb & 15) / (long long)sizeof(T));
+    float tv = lane < ntail ? Elem<T>::load1(x + r * ld + et + lane) : NAN;  // the row's ragged end
+
+    float vmx[kVecs];  // each vector's maximum (NaN when all its elements are cleared)
+#pragma unroll
+    for (int j = 0; j < kVecs; ++j) vmx[j] = Elem<T>::vmax(v[j]);
+    auto lane_max = [&]() {
+      float m = fmaxf(-INFINITY, tv);
+#pragma unroll
+      for (int j = 0; j < kVecs; ++j) m = fmaxf(m, vmx[j]);
+      return m;
+    };
+    float lm = lane_max();
+    // An element enters only above the floor f: the K-th best value held,
+    // when there is one (the held keys all come from earlier steps, with
+    // lower IDs, so only a strictly larger value can enter); else the K-th
+    // largest lane maximum, which K elements of this step reach.
+    float f = have_k ? thr : warp_kth(lm, K, lane);
+    bool strict = have_k;
+    // Each pass takes every lane's largest remaining element above the floor
+    // (the lowest ID among equal values), inserts those keys into the held
+    // list, and clears them from the registers.
+    while (__any_sync(kFull, strict ? lm > f : lm >= f)) {
+      unsigned long long key = 0ull;
+      if (strict ? lm > f : lm >= f) {
+        // the lowest vector holding the lane maximum (the tail comes last)
+        int jv = kVecs;
+#pragma unroll
+        for (int j = kVecs - 1; j >= 0; --j) jv = vmx[j] == lm ? j : jv;
+        if (jv < kVecs) {
+          uint4 w = v[0];
+#pragma unroll
+          for (int j = 1; j < kVecs; ++j) w = jv == j ? v[j] : w;
+          float e[kV];
+          Elem<T>::unpack(w, e);
+          int q0 = kV;
+#pragma unroll
+          for (int q = kV - 1; q >= 0; --q) q0 = e[q] == lm ? q : q0;
+          key = tr_key(tr_ord(lm), (uint32_t)(id0 + ((long long)jv * 32 + lane) * kV + q0));
+          w = Elem<T>::clear(w, q0);
+          const float wm = Elem<T>::vmax(w);
+#pragma unroll
+          for (int j = 0; j < kVecs; ++j) {
+            v[j] = jv == j ? w : v[j];
+            vmx[j] = jv == j ? wm : vmx[j];
+          }
+        } else {
+          key = tr_key(tr_ord(tv), (uint32_t)(et + lane));
+          tv = NAN;
+        }
+      }
+      // keys that cannot beat the K-th held key stay out
+      const unsigned long long kth0 = __shfl_sync(kFull, lk, K - 1);
+      if (key <= kth0) key = 0ull;
+      unsigned mask = __ballot_sync(kFull, key != 0ull);
+      while (mask) {
+        const int src = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const unsigned long long k = __shfl_sync(kFull, key, src);
+        // its place is the number of larger held keys; the keys below it move
+        // up one lane and the K-th falls off
+        const int pos = __popc(__ballot_sync(kFull, lk > k));
+        if (pos < K) {
+          const unsigned long long up = __shfl_up_sync(kFull, lk, 1);
+          if (lane == pos) lk = k;
+          else if (lane > pos && lane < K) lk = up;
+        }
+      }
+      const unsigned long long kth = __shfl_sync(kFull, lk, K - 1);
+      if (kth) {
+        have_k = true;
+        thr = tr_key_val(kth);
+        // keys of this step may tie the new K-th value with a lower ID
+        f = thr;
+        strict = false;
+      }
+      lm = lane_max();
+    }
+  };
+
+  long long r = u0 / nch;
+  int c = (int)(u0 - r * nch);
+  int q = 0;
+  uint32_t ph = 0;
+  int i = 0;
+  for (; i < n_steps; ++i) {
+    if (!__all_sync(kFull, mbar_wait_for(&ring.full[q], ph))) break;
+    uint4 v[kVecs];
+    fetch(v, q, r, c);
+    process(v, r, c);
+    if (++c == nch) {
+      c = 0;
+      ++r;
+    }
+    if (++q == kStages) {
+      q = 0;
+      ph ^= 1u;
+    }
+  }
+  if (i < n_steps) {
+    // a copy that never landed: flag it and wait (bounded) for this warp's
+    // other copies before the CTA's shared memory goes away
+    if (lane == 0) tr_flag(status, TR_DEV_TIMEOUT);
+    for (int j = i; j < i + kStages && j < n_steps; ++j)
+      mbar_drain(&ring.full[j % kStages], (uint32_t)((j / kStages) & 1));
+    return;
+  }
+  flush(cur);
+}
+
+// ---------------------------------------------------------------------------
+// plain scan (rows that are not 16-byte aligned)
+// ---------------------------------------------------------------------------
+
+constexpr int kThreads = 256;
+constexpr long long kScanChunk = 16384;  // elements of a row per CTA
+constexpr int kMaxCluster = 8;           // portable thread-block cluster size
+constexpr int kMaxSplits = 32;
 
 // The K largest of n distinct keys in shared memory, sorted, into out[0..K)
 // (0 where fewer than K): each key's rank is the number of larger keys.
@@ -126,14 +399,6 @@ __device__ __forceinline__ void rank_select(const unsigned long long *keys, int 
   __syncthreads();
 }
 
-// Thread-block cluster helpers: the rank of this CTA in its cluster, a store
-// into another CTA's shared memory, and the cluster-wide barrier.
-__device__ __forceinline__ unsigned cluster_rank() {
-  unsigned r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
 __device__ __forceinline__ void st_cluster_u64(void *local_addr, unsigned rank, unsigned long long v) {
   const unsigned a = (unsigned)__cvta_generic_to_shared(local_addr);
   unsigned remote;
@@ -141,23 +406,16 @@ __device__ __forceinline__ void st_cluster_u64(void *local_addr, unsigned rank, 
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
 }
 
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // CLUSTER: the row's chunks form one thread-block cluster and merge through
 // the first CTA's shared memory; otherwise through the workspace, the row's
 // last CTA to finish merging (an arrival counter, no spin-wait).
-template <typename T, int KMAX, bool VEC, bool CLUSTER>
-__global__ void __launch_bounds__(kThreads, KMAX <= 8 ? 3 : 1) topk_kernel(const T *logits, long long V, long long ld, int K,
-                                                        long long chunk, int32_t *ids, float *vals,
-                                                        unsigned long long *part, unsigned *counters) {
-  __shared__ unsigned long long keys[kRankKeys];       // candidate keys being ranked
+template <typename T, int KMAX, bool CLUSTER>
+__global__ void __launch_bounds__(kThreads) topk_scan_kernel(const T *logits, long long V, long long ld, int K,
+                                                             long long chunk, int32_t *ids, float *vals,
+                                                             unsigned long long *part, unsigned *counters) {
+  __shared__ unsigned long long keys[kMaxSplits * TR_MAX_K];
   __shared__ unsigned long long top[TR_MAX_K];
-  __shared__ unsigned long long gathered[kMaxCluster * TR_MAX_K];  // the cluster's lists (first CTA)
   __shared__ unsigned long long warp_keys[kThreads / 32][KMAX];
-  __shared__ float wfloor[kThreads / 32];
-  __shared__ int wcount[kThreads / 32];
   __shared__ int is_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, splits = gridDim.x;
@@ -166,111 +424,29 @@ __global__ void __launch_bounds__(kThreads, KMAX <= 8 ? 3 : 1) topk_kernel(const
   const long long lo = split * chunk;
   const long long hi = min(V, lo + chunk);
 
-  bool ranked = false;
-  if (VEC) {
-    // The chunk sits in registers (64 bytes a thread).  The K-th largest
-    // lane maximum of a warp is reached by at least K elements of that warp,
-    // so no element strictly below the largest such warp floor can be in the
-    // row's top K.  The elements at or above it (well under 1% of random
-    // logits) are counted, given slots by a block-wide scan, and ranked.
-    constexpr int kV = Elem<T>::kVec;
-    constexpr int NV = kWindowBytes / (kThreads * 16);
-    const uint4 *xv = reinterpret_cast<const uint4 *>(x + lo);
-    const int nvec = (int)((hi - lo) / kV);
-    uint4 buf[NV];
-#pragma unroll
-    for (int u = 0; u < NV; ++u) {
-      const int i = u * kThreads + tid;
-      buf[u] = i < nvec ? __ldcs(xv + i) : Elem<T>::nan_vec();  // NaN never passes a compare
-    }
-    // the ragged end of the chunk (fewer than one vector): one element for some threads
-    const long long tail0 = lo + (long long)nvec * kV;
-    const bool has_tail = tail0 + tid < hi;
-    const float tail_v = has_tail ? Elem<T>::load1(x + tail0 + tid) : NAN;
-    float lm = has_tail ? tail_v : -INFINITY;
-#pragma unroll
-    for (int u = 0; u < NV; ++u) lm = fmaxf(lm, Elem<T>::vmax(buf[u]));
-    const float wk = warp_kth(lm, K, lane);
-    if (lane == 0) wfloor[warp] = wk;
-    __syncthreads();
-    float floor_v = wfloor[0];
-#pragma unroll
-    for (int w = 1; w < kThreads / 32; ++w) floor_v = fmaxf(floor_v, wfloor[w]);
-    // count, then a block-wide exclusive scan of the counts
-    // (bf16: a vector whose maximum is below the floor is skipped whole)
-    int cnt = has_tail && tail_v >= floor_v;
-#pragma unroll
-    for (int u = 0; u < NV; ++u) {
-      if (!Elem<T>::kPrefilter || Elem<T>::vmax(buf[u]) >= floor_v) {
-        float e[kV];
-        Elem<T>::unpack(buf[u], e);
-#pragma unroll
-        for (int q = 0; q < kV; ++q) cnt += e[q] >= floor_v;
-      }
-    }
-    int incl = cnt;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    if (lane == 31) wcount[warp] = incl;
-    __syncthreads();
-    int base = incl - cnt, n = 0;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) {
-      const int c = wcount[w];
-      base += w < warp ? c : 0;
-      n += c;
-    }
-    if (n <= kRankKeys) {
-      // keys straight from the registers
-      if (cnt) {
-#pragma unroll
-        for (int u = 0; u < NV; ++u) {
-          if (!Elem<T>::kPrefilter || Elem<T>::vmax(buf[u]) >= floor_v) {
-            float e[kV];
-            Elem<T>::unpack(buf[u], e);
-#pragma unroll
-            for (int q = 0; q < kV; ++q)
-              if (e[q] >= floor_v) keys[base++] = tr_key(tr_ord(e[q]), (uint32_t)(lo + (u * kThreads + tid) * kV + q));
-          }
-        }
-        if (has_tail && tail_v >= floor_v) keys[base] = tr_key(tr_ord(tail_v), (uint32_t)(tail0 + tid));
-      }
-      __syncthreads();
-      rank_select(keys, n, K, top);
-      ranked = true;
-    }
-    // else: many elements tie at the floor; the plain scan below takes the chunk again
-  }
-  if (!ranked) {
-    // rows that are not 16-byte aligned (or chunks with more than kRankKeys
-    // elements at the floor): a plain scan through register lists
-    TopList<KMAX> L;
+  TopList<KMAX> L;
+  L.init();
+  for (long long i = lo + tid; i < hi; i += kThreads) L.push(Elem<T>::load1(x + i), (uint32_t)i);
+  unsigned long long mine = warp_merge<KMAX>(L, lane);
+  if (lane < KMAX) warp_keys[warp][lane] = mine;
+  __syncthreads();
+  if (warp == 0) {
     L.init();
-    for (long long i = lo + tid; i < hi; i += kThreads) L.push(Elem<T>::load1(x + i), (uint32_t)i);
-    unsigned long long mine = warp_merge<KMAX>(L, lane);
-    if (lane < KMAX) warp_keys[warp][lane] = mine;
-    __syncthreads();
-    if (warp == 0) {
-      L.init();
-      if (lane < kThreads / 32)
+    if (lane < kThreads / 32)
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) L.k[j] = warp_keys[lane][j];
-      mine = warp_merge<KMAX>(L, lane);
-      if (lane < K) top[lane] = mine;
-    }
-    __syncthreads();
+      for (int j = 0; j < KMAX; ++j) L.k[j] = warp_keys[lane][j];
+    mine = warp_merge<KMAX>(L, lane);
+    if (lane < K) top[lane] = mine;
   }
+  __syncthreads();
 
   if (CLUSTER) {
     // every chunk's list into the first CTA's shared memory, then one ranking there
-    const unsigned cr = cluster_rank();
-    if (tid < K) st_cluster_u64(&gathered[cr * K + tid], 0, top[tid]);
-    cluster_sync();
+    const unsigned cr = sm100::cluster_ctarank();
+    if (tid < K) st_cluster_u64(&keys[cr * K + tid], 0, top[tid]);
+    sm100::cluster_sync_all();
     if (cr != 0) return;
-    rank_select(gathered, splits * K, K, top);
+    rank_select(keys, splits * K, K, top);
   } else if (splits > 1) {
     // publish this chunk's top K; the row's last CTA to arrive ranks all chunks' keys
     if (tid < K) part[(row * splits + split) * KMAX + tid] = top[tid];
@@ -292,84 +468,89 @@ __global__ void __launch_bounds__(kThreads, KMAX <= 8 ? 3 : 1) topk_kernel(const
   }
 }
 
-template <typename T, int KMAX, bool VEC, bool CLUSTER>
-cudaError_t launch_one(const void *logits, long long rows, long long V, long long ld, int K, int splits, long long chunk,
-                int32_t *ids, float *vals, unsigned long long *part, unsigned *counters, cudaStream_t s) {
+// ---------------------------------------------------------------------------
+// launch
+// ---------------------------------------------------------------------------
+
+// Workspace: per-(row, step) list slots of KMAX keys (fp32 step count: the
+// most steps, so bf16 rows fit as well), then one arrival counter per row.
+size_t part_bytes_for(long long rows, long long V, int K) {
+  return tr_align_up((size_t)rows * (size_t)steps_per_row(V, 4) * tr_kmax(K) * 8, 256);
+}
+
+template <typename T, int KMAX>
+cudaError_t launch_warp(const void *logits, long long rows, long long V, long long ld, int K, int32_t *ids,
+                        float *vals, unsigned long long *part, unsigned *counters, cudaStream_t s) {
+  const int nch = (int)steps_per_row(V, sizeof(T));
+  const long long U = rows * nch;
+  const long long want = (U + kWarps - 1) / kWarps;
+  const long long most = tr_sm_count();  // one CTA per SM, persistent
+  const int grid = (int)(want < most ? want : most);
+  static bool attr_set[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(topk_warp_kernel<T, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  topk_warp_kernel<T, KMAX><<<grid, kWarps * 32, kRingSmem, s>>>((const T *)logits, V, ld, K, nch, U, ids, vals, part,
+                                                                 counters, tr_status_dev());
+  return cudaGetLastError();
+}
+
+template <typename T, int KMAX>
+cudaError_t launch_scan(const void *logits, long long rows, long long V, long long ld, int K, int32_t *ids,
+                        float *vals, unsigned long long *part, unsigned *counters, cudaStream_t s) {
+  long long splits = (V + kScanChunk - 1) / kScanChunk;
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  const long long chunk = (V + splits - 1) / splits;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(splits, (unsigned)rows);
+  cfg.gridDim = dim3((unsigned)splits, (unsigned)rows);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  if (CLUSTER) {
+  const bool cluster = splits > 1 && splits <= kMaxCluster;
+  if (cluster) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)splits;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_scan_kernel<T, KMAX, true>, (const T *)logits, V, ld, K, chunk, ids, vals,
+                              part, counters);
   }
-  return cudaLaunchKernelEx(&cfg, topk_kernel<T, KMAX, VEC, CLUSTER>, (const T *)logits, V, ld, K, chunk, ids, vals,
+  return cudaLaunchKernelEx(&cfg, topk_scan_kernel<T, KMAX, false>, (const T *)logits, V, ld, K, chunk, ids, vals,
                             part, counters);
 }
 
 template <typename T, int KMAX>
-cudaError_t launch(const void *logits, long long rows, long long V, long long ld, int K, int splits, long long chunk,
-            bool vec, int32_t *ids, float *vals, void *ws, size_t part_bytes, cudaStream_t s) {
+cudaError_t launch(const void *logits, long long rows, long long V, long long ld, int K, int32_t *ids, float *vals,
+                   void *ws, cudaStream_t s) {
   unsigned long long *part = (unsigned long long *)ws;
-  unsigned *counters = (unsigned *)((char *)ws + part_bytes);
-  const bool cluster = splits > 1 && splits <= kMaxCluster;
-  if (vec)
-    return cluster ? launch_one<T, KMAX, true, true>(logits, rows, V, ld, K, splits, chunk, ids, vals, part, counters, s)
-                   : launch_one<T, KMAX, true, false>(logits, rows, V, ld, K, splits, chunk, ids, vals, part, counters, s);
-  return cluster ? launch_one<T, KMAX, false, true>(logits, rows, V, ld, K, splits, chunk, ids, vals, part, counters, s)
-                 : launch_one<T, KMAX, false, false>(logits, rows, V, ld, K, splits, chunk, ids, vals, part, counters, s);
-}
-
-long long plan_chunk(long long V, int splits) {
-  // chunks are multiples of 8 elements so every chunk of an aligned row is 16-byte aligned
-  long long c = (V + splits - 1) / splits;
-  return (c + 7) / 8 * 8;
-}
-
-size_t part_bytes_for(long long rows, int splits, int K) {
-  return splits > 1 ? tr_align_up((size_t)rows * splits * tr_kmax(K) * 8, 256) : 0;
+  unsigned *counters = (unsigned *)((char *)ws + (ws ? part_bytes_for(rows, V, K) : 0));
+  const bool aligned = ((uintptr_t)logits % 16 == 0) && ((ld * (long long)sizeof(T)) % 16 == 0);
+  if (aligned) return launch_warp<T, KMAX>(logits, rows, V, ld, K, ids, vals, part, counters, s);
+  return launch_scan<T, KMAX>(logits, rows, V, ld, K, ids, vals, part, counters, s);
 }
 
 }  // namespace
 
-// Chunks per row for elements of esz bytes; the workspace is laid out for
-// fp32 (the most chunks), so it also fits bf16 rows.
-static int plan_splits(int64_t V, size_t esz) {
-  const long long per = kWindowBytes / (long long)esz;
-  long long s = (V + per - 1) / per;
-  if (s < 1) s = 1;
-  if (s > kMaxSplits) s = kMaxSplits;
-  return (int)s;
-}
-
-int tr_topk_plan_splits(int64_t rows, int64_t V) {
-  (void)rows;
-  return plan_splits(V, 4);
-}
-
 extern "C" size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K) {
   if (rows <= 0 || V <= 0 || K < 1 || K > TR_MAX_K) return 0;
-  const int splits = tr_topk_plan_splits(rows, V);
-  if (splits == 1) return 0;
-  return part_bytes_for(rows, splits, K) + tr_align_up((size_t)rows * 4, 256);
+  if (steps_per_row(V, 4) == 1) return 0;  // no row is ever split
+  return part_bytes_for(rows, V, K) + tr_align_up((size_t)rows * 4, 256);
 }
+
+size_t tr_topk_counters_offset(int64_t rows, int64_t V, int K) { return part_bytes_for(rows, V, K); }
 
 int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K, int32_t *ids,
                    float *vals, void *ws, size_t ws_bytes, cudaStream_t s) {
-  const size_t esz = ftype == TR_F32 ? 4 : 2;
-  const int splits = plan_splits(V, esz);
-  const long long chunk = splits > 1 ? plan_chunk(V, splits) : V;
-  const bool vec = ((uintptr_t)logits % 16 == 0) && ((ld * (int64_t)esz) % 16 == 0) &&
-                   chunk <= kWindowBytes / (long long)esz;
-  // the partial lists are laid out for the fp32 chunk count (never fewer chunks)
-  const size_t pb = part_bytes_for(rows, tr_topk_plan_splits(rows, V), K);
+  (void)ws_bytes;
   const int km = tr_kmax(K);
-#define TR_TOPK_CASE(T, KM) launch<T, KM>(logits, rows, V, ld, K, splits, chunk, vec, ids, vals, ws, pb, s)
+#define TR_TOPK_CASE(T, KM) launch<T, KM>(logits, rows, V, ld, K, ids, vals, ws, s)
   cudaError_t e;
   if (ftype == TR_F32)
     e = km == 8 ? TR_TOPK_CASE(float, 8) : km == 16 ? TR_TOPK_CASE(float, 16) : TR_TOPK_CASE(float, 32);
@@ -379,7 +560,6 @@ int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, 
 #undef TR_TOPK_CASE
   if (e != cudaSuccess) return TR_E_CUDA;
   TR_LAUNCH_CHECK();
-  (void)ws_bytes;
   return TR_OK;
 }
 
@@ -392,7 +572,7 @@ extern "C" int tr_topk(const void *logits, tr_ftype ftype, int64_t rows, int64_t
   if (!logits || !ids) return TR_E_INVAL;
   const size_t need = tr_topk_workspace_bytes(rows, V, K);
   if (need && (!ws || ws_bytes < need)) return TR_E_INVAL;
-  if (rows > 65535) return TR_E_UNSUPPORTED;  // grid.y limit
+  if (rows > 65535) return TR_E_UNSUPPORTED;  // grid.y limit of the plain scan
   int rc = tr_check_device();
   if (rc != TR_OK) return rc;
   return tr_topk_launch(logits, ftype, rows, V, ld, K, ids, vals, ws, ws_bytes, (cudaStream_t)stream);

@@ -55,8 +55,7 @@ extern "C" int tr_topk_noalloc(const void *logits, tr_ftype ftype, int64_t rows,
   if (need) {
     // the arrival counters sit after the partial lists and must start at zero;
     // the array keeps whatever the previous call left there
-    const int splits = tr_topk_plan_splits(rows, V);
-    const size_t part = tr_align_up((size_t)rows * splits * tr_kmax(K) * 8, 256);
+    const size_t part = tr_topk_counters_offset(rows, V, K);
     if (cudaMemsetAsync((char *)scratch + part, 0, need - part, s) != cudaSuccess) return TR_E_CUDA;
   }
   return tr_topk_launch(logits, ftype, rows, V, ld, K, ids, vals, scratch, (size_t)TR_TOPK_NOALLOC_SCRATCH_BYTES, s);

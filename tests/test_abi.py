@@ -87,11 +87,14 @@ def test_host_validation_before_any_launch(lib):
 
 def test_workspace_sizes(lib):
     import free_speculative_decoding_gb300 as tr
-    # rows that fit one 16K-element chunk need no workspace; longer rows need a
-    # K-key list per chunk (8-byte keys) and a counter per row
-    assert lib.tr_topk_workspace_bytes(10, 16384, 8) == 0
-    assert lib.tr_topk_workspace_bytes(1280, 32000, 8) >= 1280 * 2 * 8 * 8 + 1280 * 4
-    assert lib.tr_topk_workspace_bytes(1024, 128256, 8) >= 1024 * 8 * 8 * 8 + 1024 * 4
+    # rows of at most one 8 KB unit (2048 fp32 elements) are never split and
+    # need no workspace; longer rows need a K-key list slot per unit (8-byte
+    # keys, 16 units for a 32000-entry fp32 row) and a counter per row
+    assert lib.tr_topk_workspace_bytes(10, 2048, 8) == 0
+    assert lib.tr_topk_workspace_bytes(10, 2049, 8) > 0
+    assert lib.tr_topk_workspace_bytes(1280, 32000, 8) >= 1280 * 16 * 8 * 8 + 1280 * 4
+    assert lib.tr_topk_workspace_bytes(1024, 128256, 8) >= 1024 * 63 * 8 * 8 + 1024 * 4
+    assert lib.tr_topk_workspace_bytes(33, 20000, 16) >= 33 * 10 * 16 * 8 + 33 * 4
     t = tr.Tree(synth.TREE_T80, 8)
     assert lib.tr_verify_attn_workspace_bytes(16, 32, 32, 128, 5888, t.handle) > 0
     assert lib.tr_kv_commit_workspace_bytes(16) >= 64

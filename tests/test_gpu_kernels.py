@@ -157,14 +157,44 @@ def test_topk_matches_oracle(tr, V, rows, K, dtype):
     _status_ok(tr)
 
 
-def test_topk_strided_rows_and_empty(tr):
-    x = torch.randn(9, 5003)
-    ids_ref, _ = oracle.topk_rows(x[:, :4999].numpy(), 8)
+@pytest.mark.parametrize("ld", [5003, 5004])
+def test_topk_strided_rows_and_empty(tr, ld):
+    # ld = 5003: rows not 16-byte aligned (plain scan); ld = 5004: aligned rows
+    # whose last 12 bytes lie past the last whole 16-byte vector
+    x = torch.randn(9, ld)
+    ids_ref, vals_ref = oracle.topk_rows(x[:, :4999].numpy(), 8)
     ids = torch.zeros(9, 8, dtype=torch.int32, device="cuda")
-    tr.tr_topk(x.cuda(), 8, ids, None, tr.workspace(0), V=4999)     # ld = 5003, unaligned rows
+    vals = torch.zeros(9, 8, dtype=torch.float32, device="cuda")
+    x[:, 4999:] = 100.0   # beyond V: must never be read as a candidate
+    tr.tr_topk(x.cuda(), 8, ids, vals, tr.workspace(tr.tr_topk_workspace_bytes(9, 4999, 8)), V=4999)
     assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.array_equal(vals.cpu().numpy(), vals_ref.astype(np.float32))
     e = torch.zeros(0, 100, device="cuda")
     tr.tr_topk(e, 4, torch.zeros(0, 4, dtype=torch.int32, device="cuda"), None, None)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_topk_all_equal_and_few_values(tr, dtype):
+    # every element ties: far more candidates than the shared-memory ranking
+    # holds, so the register-list path decides; the K lowest IDs win
+    rows, V, K = 6, 40000, 8
+    x = torch.zeros(rows, V)
+    x[1] = 1.5
+    x[2, ::2] = 1.0                     # half the row at the maximum
+    g = torch.Generator().manual_seed(5)
+    x[3] = torch.randint(0, 3, (V,), generator=g).float()   # three values
+    x[4, 30000:] = 2.0                  # the maximum only in late units
+    x[5, -1] = 7.0                      # the best element is the very last one
+    x = x.to(dtype)
+    ids_ref, vals_ref = oracle.topk_rows(x.float().numpy(), K)
+    ids = torch.zeros(rows, K, dtype=torch.int32, device="cuda")
+    vals = torch.zeros(rows, K, dtype=torch.float32, device="cuda")
+    ws = tr.workspace(tr.tr_topk_workspace_bytes(rows, V, K))
+    for _ in range(2):
+        tr.tr_topk(x.cuda(), K, ids, vals, ws)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        assert np.array_equal(vals.cpu().numpy(), vals_ref.astype(np.float32))
+    _status_ok(tr)
 
 
 # ----------------------------------------------------------------------------
@@ -323,21 +353,28 @@ def test_attention_matches_oracle(tr, tree_name, B, Hq, Hkv, lens):
 # fused LM head + top-K
 # ----------------------------------------------------------------------------
 
-def test_lmhead_exact_grid_workload(tr):
+@pytest.mark.parametrize("rows,D,V,sample", [
+    (200, 1024, 5000, None),      # one row tile, both halves partly past the rows
+    (600, 512, 9001, None),       # three row tiles, a ragged last column tile
+    (2560, 4096, 32000, 97),      # the full LM-head workload, every 97th row checked
+])
+def test_lmhead_exact_grid_workload(tr, rows, D, V, sample):
     w = synth.WORKLOADS["lmhead"]
-    rows, D, V, K = 200, 1024, 5000, 8
+    K = 8
     tok = np.arange(rows) * 37 % V
     H = synth.lm_hidden_rows(w.seed, 0, np.arange(rows), tok, D)
     Wt = synth.lm_weight_rows(w.seed, V, D)
-    ref = oracle.lmhead_logits(synth.bf16_to_f32(H), synth.bf16_to_f32(Wt))
+    check = np.arange(rows) if sample is None else np.arange(0, rows, sample)
+    ref = oracle.lmhead_logits(synth.bf16_to_f32(H[check]), synth.bf16_to_f32(Wt))
     ids_ref, vals_ref = oracle.topk_rows(ref, K)
     ids = torch.zeros(rows, K, dtype=torch.int32, device="cuda")
     vals = torch.zeros(rows, K, dtype=torch.float32, device="cuda")
     ws = tr.workspace(tr.tr_lmhead_topk_workspace_bytes(rows, D, V, K))
     tr.tr_lmhead_topk(bf16_tensor(H), bf16_tensor(Wt), K, ids, vals, ws)
     # products and partial sums are exact in fp32 on this grid, so the result is exact
-    assert np.array_equal(ids.cpu().numpy(), ids_ref)
-    assert np.array_equal(vals.cpu().numpy().astype(np.float64), vals_ref)
+    assert np.array_equal(ids.cpu().numpy()[check], ids_ref)
+    assert np.array_equal(vals.cpu().numpy()[check].astype(np.float64), vals_ref)
+    _status_ok(tr)
 
 
 def test_lmhead_tolerance_rule_off_grid(tr):
