@@ -11,7 +11,12 @@
 //               and one elected lane issues;
 //   warps 2..5  epilogue: each thread owns one TMEM lane (one hidden row) and
 //               streams the tile's 256 fp32 logits from TMEM into a register
-//               top-K list, then writes that list (one per row and tile).
+//               top-K list, then writes that list (one per row and tile).  Per
+//               32-column chunk each lane marks the columns that can enter its
+//               list; a chunk with any such column is staged in shared memory
+//               and every lane walks only its own marks, so a warp pays for
+//               its busiest row's insertions instead of one insertion per
+//               column for all 32 rows.
 // A second kernel merges each row's per-tile lists into the final top-K.  The
 // two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
 //
@@ -27,7 +32,8 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int kThreads = 192;
-constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int kStageFloats = 128 * 33;  // epilogue: 32 logits per row, padded
+constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + 1024 + 256 + kStageFloats * 4;
 constexpr uint32_t kIdesc = sm100::idesc_bf16_f32(BM, BN);
 
 struct Bars {
@@ -44,6 +50,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Bars *bars = (Bars *)(smem + STAGES * STAGE_BYTES);
+  float *stage = (float *)(smem + STAGES * STAGE_BYTES + 256);
   volatile int *abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = n_mt * n_nt;
@@ -166,14 +173,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       L.init();
       const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN);
       const long long col0 = (long long)nt * BN;
+      float *mine = stage + (threadIdx.x - 64) * 33;  // this row's 32 staged logits (stride 33: no bank conflicts)
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         float v[32];
         tmem_ld32(taddr + c0, v);
+        // columns that can enter this row's list (none past the vocabulary)
+        const int n_in = (int)min((long long)32, V - (col0 + c0));
+        uint32_t m = 0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const long long col = col0 + c0 + j;
-          if (col < V) L.push(v[j], (uint32_t)col);
+        for (int j = 0; j < 32; ++j) m |= (uint32_t)(j < n_in && v[j] >= L.thr) << j;
+        if (__any_sync(0xffffffffu, m != 0u)) {
+          // each lane walks only its own candidates, so the warp's cost is the
+          // busiest row's candidate count rather than every column
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mine[j] = v[j];  // lane-private: no barrier needed
+          while (m) {
+            const int j = __ffs(m) - 1;
+            m &= m - 1;
+            L.push(mine[j], (uint32_t)(col0 + c0 + j));
+          }
         }
       }
       tc_fence_before();
