@@ -16,7 +16,8 @@
 //               list; a chunk with any such column is staged in shared memory
 //               and every lane walks only its own marks, so a warp pays for
 //               its busiest row's insertions instead of one insertion per
-//               column for all 32 rows.
+//               column for all 32 rows.  A first read of the tile sets each
+//               list's floor to the smallest of KMAX column-group maxima.
 // A second kernel merges each row's per-tile lists into the final top-K.  The
 // two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
 //
@@ -174,6 +175,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN);
       const long long col0 = (long long)nt * BN;
       float *mine = stage + (threadIdx.x - 64) * 33;  // this row's 32 staged logits (stride 33: no bank conflicts)
+      {
+        // a first read of the tile: the smallest of KMAX group maxima is
+        // reached by KMAX elements of this row, so nothing below it can enter
+        constexpr int GW = BN / KMAX;  // columns per group
+        float fl = INFINITY;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + c0, v);
+          const int n_in = (int)min((long long)32, V - (col0 + c0));
+#pragma unroll
+          for (int g = 0; g < 32 / GW; ++g) {
+            float gm = -INFINITY;
+#pragma unroll
+            for (int j = g * GW; j < (g + 1) * GW; ++j) gm = j < n_in ? fmaxf(gm, v[j]) : gm;
+            fl = fminf(fl, gm);
+          }
+        }
+        L.raise_floor(fl);
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         float v[32];
