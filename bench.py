@@ -144,6 +144,34 @@ def topk_bytes(w, N):
     return w.B * N * w.V * esz
 
 
+def workload_of(args):
+    """The named workload, with the draft tree of --tree if given."""
+    w = synth.WORKLOADS[args.workload]
+    return w.scaled(tree=args.tree) if args.tree else w
+
+
+def rank_workload(w, rank, world):
+    """The workload of one rank: each rank decodes its own sequences (the seed
+    moves with the rank); shapes are the same on every rank."""
+    return w.scaled(seed=w.seed + 1000 * rank) if world > 1 else w
+
+
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values (the job's time is its slowest rank)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, steps, total_ms):
+    """Whole-job steps/s: every rank ran `steps` steps of its own batch within total_ms."""
+    return world * steps * 1e3 / total_ms
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -151,9 +179,7 @@ def run_gpu(args, rank, world):
     from free_speculative_decoding_gb300.engine import TRState
     from synth import device as sd
 
-    w = synth.WORKLOADS[args.workload]
-    if world > 1:
-        w = w.scaled(seed=w.seed + 1000 * rank)   # each rank decodes its own sequences
+    w = rank_workload(workload_of(args), rank, world)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     tree = tr.Tree(w.child_counts, w.K)
@@ -316,10 +342,7 @@ def run_gpu(args, rank, world):
             torch.cuda.synchronize()
             topk_ms = [e0.elapsed_time(e1) for e0, e1 in tev]
 
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     res = {"total_ms": total_ms, "attn_ms": attn_ms, "attn_bytes": attn_bytes_list, "replay_ok": replay_ok,
            "status": status, "clocks": clk, "committed": committed, "N": N, "w": w, "seg": seg,
@@ -352,9 +375,10 @@ def run_e2e(args, w, st, tgt, bufs, gen_step, hot_step, snapshot, restore, dev, 
     h2d = sum(host[k][0].numel() * host[k][0].element_size() for k in host)
     d2h = out_acc[0].numel() * 4 + out_com[0].numel() * 4
     stream = torch.cuda.current_stream()
-    copy_stream = torch.cuda.Stream(device=dev)
     # two device slots: a copy stream brings step i+1's inputs in while step i
-    # runs; slot reuse waits for the step that last read it
+    # runs; slot reuse waits for the step that last read it (splitting the
+    # copy over several streams measured no faster)
+    copy_stream = torch.cuda.Stream(device=dev)
     slots = 2 if bufs["H" if lm else "logits"].shape[0] >= 2 else 1
     copied = [torch.cuda.Event() for _ in range(E)]
     used = [torch.cuda.Event() for _ in range(E)]
@@ -473,6 +497,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", default="tr", choices=["tr", "reference"])
     ap.add_argument("--workload", default="batched", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tree", default=None, choices=sorted(synth.TREES),
+                    help="draft tree in place of the workload's own (the tree-shape sweep)")
     ap.add_argument("--store-gb", type=float, default=40.0, help="HBM for recorded step inputs")
     ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
@@ -480,7 +506,7 @@ def main():
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     metric = "TR steps/s"
     unit = "steps/s (%d sequences x %d-node tree per step)" % (w.B, w.N)
 
@@ -519,7 +545,7 @@ def main():
     wl = res["w"]
     N = res["N"]
     ms_per_step = res["total_ms"] / K
-    value = world * 1e3 / ms_per_step       # whole-job steps/s (each rank its own batch)
+    value = job_rate(world, K, res["total_ms"])   # whole-job steps/s (each rank its own batch)
     peaks, peak_kind = load_peaks()
     roofline = None
     if wl.attention and res["attn_ms"]:
@@ -546,7 +572,8 @@ def main():
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 attention (fp32 accumulate), %s logits, int64/int32 state" % wl.logits,
         "data": "synthetic (seeded splitmix64 target; see DESIGN.md)",
-        "config": {"workload": args.workload, "B": wl.B, "V": wl.V, "K": wl.K, "tree_nodes": N,
+        "config": {"workload": args.workload, "B": wl.B, "V": wl.V, "K": wl.K, "tree": wl.tree, "tree_nodes": N,
+                   "tree_depth": wl.depth(),
                    "prefix": list(wl.prefix), "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
                    "parallelism": "replicas (dp%d, no collective)" % world,
                    "l2": "per-step inputs larger than L2 (fresh logits + KV cache)",

@@ -9,8 +9,10 @@
 // cut into equal contiguous ranges, one per warp of a persistent grid (one
 // CTA of 8 warps per SM).  Each warp pulls its steps through a private ring
 // of three bulk copies (cp.async.bulk into shared memory, completing on an
-// mbarrier), copies the step at hand into registers, and keeps the current
-// row's running top-K across its lanes (lane j holds the j-th best key).
+// mbarrier) and examines each step where it landed: vector maxima are read
+// from the stage, an element handed over is cleared there, and the stage is
+// refilled once the step is done.  The warp keeps the current row's running
+// top-K across its lanes (lane j holds the j-th best key).
 // Only elements above a floor can enter: the K-th best value held, or on a
 // segment's first step the K-th largest lane maximum.  A step with no lane
 // maximum above the floor costs a vector maximum and one vote; otherwise each
@@ -229,29 +231,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   if (lane == 0)
     for (int q = 0; q < kStages && q < n_steps; ++q) issue(q);
 
-  // stage q's step (row r, step c of the row) into v, NaN past the row's last
-  // whole vector; then the stage takes the next step to fetch
-  auto fetch = [&](uint4 (&v)[kVecs], int q, long long r, int c) {
-    const int nvec = (int)(min(row_bytes - (long long)c * kStep, (long long)kStep) >> 4);
-    const uint4 *sv = reinterpret_cast<const uint4 *>(ring.stage[q]);
-    if (nvec == 32 * kVecs) {
-#pragma unroll
-      for (int j = 0; j < kVecs; ++j) v[j] = sv[j * 32 + lane];
-    } else {
-#pragma unroll
-      for (int j = 0; j < kVecs; ++j) {
-        const int i = j * 32 + lane;
-        v[j] = i < nvec ? sv[i] : Elem<T>::nan_vec();  // NaN never passes a compare
-      }
-    }
+  // after the step is examined (its stage read and partly cleared): the
+  // stage takes the next step to fetch
+  auto refill = [&](int q) {
     __syncwarp();
     if (lane == 0) {
-      fence_proxy_async_smem();  // the stage's reads come before the next copy into it
+      fence_proxy_async_smem();  // the stage's generic reads and writes come before the next copy into it
       if (n_issued < n_steps) issue(q);
     }
   };
 
-  auto process = [&](uint4 (&v)[kVecs], long long r, int c) {
+  auto process = [&](int q, long long r, int c) {
     if (r != cur) {
       if (cur >= 0) flush(cur);
       cur = r;
@@ -268,9 +258,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     const int ntail = (int)((nb & 15) / (long long)sizeof(T));
     float tv = lane < ntail ? Elem<T>::load1(x + r * ld + et + lane) : NAN;  // the row's ragged end
 
-    float vmx[kVecs];  // each vector's maximum (NaN when all its elements are cleared)
+    // The step stays in the warp's stage until the refill: vector maxima come
+    // straight from it, and an element handed over is cleared there (NaN).
+    uint4 *sv = reinterpret_cast<uint4 *>(ring.stage[q]);
+    const int nvec = (int)(nb >> 4);
+    float vmx[kVecs];  // each vector's maximum (NaN when none of it can enter)
+    if (nvec == 32 * kVecs) {
 #pragma unroll
-    for (int j = 0; j < kVecs; ++j) vmx[j] = Elem<T>::vmax(v[j]);
+      for (int j = 0; j < kVecs; ++j) vmx[j] = Elem<T>::vmax(sv[j * 32 + lane]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kVecs; ++j) vmx[j] = j * 32 + lane < nvec ? Elem<T>::vmax(sv[j * 32 + lane]) : NAN;
+    }
     auto lane_max = [&]() {
       float m = fmaxf(-INFINITY, tv);
 #pragma unroll
@@ -295,22 +294,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
         for (int j = kVecs - 1; j >= 0; --j) jv = vmx[j] == lm ? j : jv;
         if (jv < kVecs) {
-          uint4 w = v[0];
-#pragma unroll
-          for (int j = 1; j < kVecs; ++j) w = jv == j ? v[j] : w;
+          uint4 w = sv[jv * 32 + lane];
           float e[kV];
           Elem<T>::unpack(w, e);
           int q0 = kV;
 #pragma unroll
-          for (int q = kV - 1; q >= 0; --q) q0 = e[q] == lm ? q : q0;
+          for (int qq = kV - 1; qq >= 0; --qq) q0 = e[qq] == lm ? qq : q0;
           key = tr_key(tr_ord(lm), (uint32_t)(id0 + ((long long)jv * 32 + lane) * kV + q0));
           w = Elem<T>::clear(w, q0);
+          sv[jv * 32 + lane] = w;
           const float wm = Elem<T>::vmax(w);
 #pragma unroll
-          for (int j = 0; j < kVecs; ++j) {
-            v[j] = jv == j ? w : v[j];
-            vmx[j] = jv == j ? wm : vmx[j];
-          }
+          for (int j = 0; j < kVecs; ++j) vmx[j] = j == jv ? wm : vmx[j];
         } else {
           key = tr_key(tr_ord(tv), (uint32_t)(et + lane));
           tv = NAN;
@@ -352,9 +347,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   int i = 0;
   for (; i < n_steps; ++i) {
     if (!__all_sync(kFull, mbar_wait_for(&ring.full[q], ph))) break;
-    uint4 v[kVecs];
-    fetch(v, q, r, c);
-    process(v, r, c);
+    process(q, r, c);
+    refill(q);
     if (++c == nch) {
       c = 0;
       ++r;

@@ -144,7 +144,25 @@ TREE_T128 = _levels(
     [(0, 6)],
 )
 
-TREES = {"T80": TREE_T80, "T128": TREE_T128}
+# Tree-shape sweep at the same 80-node budget (breadth against depth).
+# W80: wide and shallow, depth 3 (level sizes 1, 8, 32, 39).
+TREE_W80 = _levels(
+    [(8, 1)],
+    [(4, 8)],
+    [(2, 7), (1, 25)],
+    [(0, 39)],
+)
+
+# D80: narrow and deep, depth 11 (level sizes 1, 4, then 8 for nine levels, 3).
+TREE_D80 = _levels(
+    [(4, 1)],
+    [(2, 4)],
+    *([[(1, 8)]] * 8),
+    [(1, 3), (0, 5)],
+    [(0, 3)],
+)
+
+TREES = {"T80": TREE_T80, "T128": TREE_T128, "W80": TREE_W80, "D80": TREE_D80}
 
 
 def chain_tree(depth):

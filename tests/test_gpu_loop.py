@@ -58,6 +58,13 @@ def test_tiny_loop_full_config():
     assert mat > 1.5   # acceptance is nontrivial on this target
 
 
+@pytest.mark.parametrize("tree", ["W80", "D80"])
+def test_tree_shape_sweep_loop(tree):
+    """The sweep's wide and deep 80-node trees through the same loop."""
+    w = synth.WORKLOADS["tiny"].scaled(tree=tree, steps=8)
+    _check_loop(w, w.steps)
+
+
 def test_batched_reduced():
     """Sequences with their own matrices and ragged prefixes (1k..4k)."""
     w = synth.WORKLOADS["batched"].scaled(B=3, steps=10)

@@ -66,3 +66,24 @@ def test_lmhead_operands_are_exact_on_grid():
     wt = synth.bf16_to_f32(synth.lm_weight_rows(5, V, D))
     assert np.array_equal(wt * 1024, np.rint(wt * 1024))
     assert np.abs(wt).max() * 1024 <= 256
+
+
+def test_tree_shape_sweep_trees():
+    """The sweep's trees share the 80-node budget: wide (depth 3) and deep
+    (depth 11) against T80 (depth 6); per-level child counts never increase
+    in BFS order, so the first of equal-token siblings has the largest subtree."""
+    import collections
+    import oracle
+    want = {"T80": (6, [1, 8, 20, 20, 15, 10, 6]), "W80": (3, [1, 8, 32, 39]),
+            "D80": (11, [1, 4] + [8] * 9 + [3])}
+    for name, (depth, sizes) in want.items():
+        counts = synth.TREES[name]
+        plan = oracle.TreePlan(counts, 8)
+        assert plan.N == 80 and plan.max_depth == depth
+        per = collections.Counter(plan.depth)
+        assert [per[d] for d in range(depth + 1)] == sizes
+        for d in range(depth + 1):
+            level = [counts[n] for n in range(plan.N) if plan.depth[n] == d]
+            assert level == sorted(level, reverse=True)
+        w = synth.WORKLOADS["batched"].scaled(tree=name)
+        assert w.N == 80 and w.depth() == depth
