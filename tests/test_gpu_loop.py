@@ -164,3 +164,54 @@ def test_gqa_full_size_losslessness():
     ref = oracle.tree_attention(synth.bf16_to_f32(q[3]), st0.kc, st0.vc, st0.L, synth.bf16_to_f32(kt[3]),
                                 synth.bf16_to_f32(vt[3]), plan, w.d ** -0.5)
     assert rows_rel_err(recs[0]["O"][0], ref) <= ATTN_TOL
+
+
+def test_long_full_size_samples_and_losslessness():
+    """4 sequences x prefix 32768, 128-node tree (the long-context workload at
+    its full batch, in the benchmark's launch configuration): losslessness on
+    every sequence, attention of two sampled heads of one sequence at step 0."""
+    w = synth.WORKLOADS["long"].scaled(steps=10)
+    b = 2
+    recs, st, status = run_gpu_loop(w, w.steps, keep_M_every=0, o_seqs=[b], o_steps={0})
+    assert status == 0
+    L0, roots = w.prefix_lengths(), synth.initial_roots(w)
+    for bb in range(w.B):
+        em = _emitted(recs, bb)
+        assert len(em) >= w.steps
+        assert _greedy_ok(w, bb, em, int(L0[bb]), int(roots[bb]))
+    plan = oracle.TreePlan(w.child_counts, w.K)
+    q, kt, vt = synth.step_qkv(w, 0, [b])
+    L = int(L0[b])
+    pos = np.arange(L)
+    for h in (0, 17):
+        kc = synth.bf16_to_f32(synth.kc_rows(w.seed, b, np.full(L, h), pos, w.d)).reshape(1, L, w.d)
+        vc = synth.bf16_to_f32(synth.vc_rows(w.seed, b, np.full(L, h), pos, w.d)).reshape(1, L, w.d)
+        ref = oracle.tree_attention(synth.bf16_to_f32(q[0][:, h:h + 1]), kc, vc, L,
+                                    synth.bf16_to_f32(kt[0][:, h:h + 1]), synth.bf16_to_f32(vt[0][:, h:h + 1]),
+                                    plan, w.d ** -0.5)
+        assert rows_rel_err(recs[0]["O"][0][:, h:h + 1], ref) <= ATTN_TOL
+
+
+def test_lmhead_full_size_losslessness_and_replay():
+    """32 sequences x 80 nodes = 2560 LM-head rows per step (the fused LM-head
+    workload at its full size): losslessness on sampled sequences and the
+    full integer replay of one sequence."""
+    w = synth.WORKLOADS["lmhead"].scaled(steps=5)
+    recs, st, status = run_gpu_loop(w, w.steps, keep_M_every=w.steps)
+    assert status == 0
+    target = target_fn(w)
+    L0, roots = w.prefix_lengths(), synth.initial_roots(w)
+    for bb in (0, 31):
+        def top1(pos, x, bb=bb):
+            return int(np.argmax(target(bb, pos, [x])[0]))
+        em = _emitted(recs, bb)
+        assert em == oracle.greedy_decode(top1, int(roots[bb]), int(L0[bb]), len(em))
+    b = 13
+    plan = oracle.TreePlan(w.child_counts, w.K)
+    states = oracle_states(w, [b], with_cache=False)
+
+    def on_step(s, i, rec):
+        compare_step(w, plan, s, i, b, rec, recs[s], attn=False)
+
+    oracle.tr_loop(plan, states, target, w.steps, w.K, qkv=None, on_step=on_step, seqs=[b])
+    assert np.array_equal(recs[-1]["M"][b], states[0].M)
