@@ -8,8 +8,9 @@
 // Work decomposition (stream-K): a "pair" is (sequence, KV head, group of MT
 // query heads); its keys are ceil(L/64) cache tiles of 64 keys followed by
 // ceil(N/64) tree tiles.  All pairs' tiles form one sequence that is cut into
-// equal contiguous ranges, one per CTA (one CTA per SM), so every SM streams
-// the same number of K/V bytes whatever the mix of prefix lengths.  A pair
+// equal contiguous ranges, one per CTA (one CTA per SM, fewer for a small
+// batch), so every SM streams the same number of K/V bytes whatever the mix
+// of prefix lengths.  A pair
 // that lies inside one range is finished in place; a pair cut by range
 // boundaries leaves an (m, l, O) partial per part (two slots per CTA), and the
 // part that finishes last merges them.
@@ -698,9 +699,20 @@ size_t smem_bytes() {
 }
 
 struct Plan {
-  int G, MT, HG, pairs, grid;
+  int G, MT, HG, pairs, grid;  // grid: CTAs the workspace is laid out for (one per SM)
   size_t o_off, ml_off, cnt_off, total;
 };
+
+// CTAs to launch: one per SM, but never so many that a CTA gets fewer than
+// kMinTiles tiles of the largest possible work (cap keys per sequence): a
+// small batch would otherwise cut every pair into many parts, each paying the
+// start-up and the partial merge.
+constexpr long long kMinTiles = 16;
+int launch_grid(const Plan &p, int B, int Hkv, int cap, int N) {
+  const long long most = (long long)B * Hkv * p.HG * ((cap + BN - 1) / BN + (N + BN - 1) / BN);
+  const long long want = (most + kMinTiles - 1) / kMinTiles;
+  return (int)std::max<long long>(1, std::min<long long>(p.grid, want));
+}
 
 Plan make_plan(int B, int Hq, int Hkv, int N) {
   Plan p;
@@ -780,6 +792,7 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
   a.t_rows = (int)t_rows;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = (cudaStream_t)stream;
+  const int grid = launch_grid(p, B, Hkv, cap, N);
   static bool attr_set[2][64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -789,14 +802,14 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
                                        (int)smem_bytes<1>()));
       attr_set[0][dev] = true;
     }
-    attn_tc_kernel<1><<<p.grid, Cfg<1>::THREADS, smem_bytes<1>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
+    attn_tc_kernel<1><<<grid, Cfg<1>::THREADS, smem_bytes<1>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
   } else {
     if (dev >= 0 && dev < 64 && !attr_set[1][dev]) {
       TR_TRY_CUDA(cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem_bytes<2>()));
       attr_set[1][dev] = true;
     }
-    attn_tc_kernel<2><<<p.grid, Cfg<2>::THREADS, smem_bytes<2>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
+    attn_tc_kernel<2><<<grid, Cfg<2>::THREADS, smem_bytes<2>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
   }
   TR_LAUNCH_CHECK();
   return TR_OK;
