@@ -10,10 +10,13 @@
 // ceil(N/64) tree tiles.  All pairs' tiles form one sequence that is cut into
 // equal contiguous ranges, one per CTA (one CTA per SM, fewer for a small
 // batch), so every SM streams the same number of K/V bytes whatever the mix
-// of prefix lengths.  A pair
-// that lies inside one range is finished in place; a pair cut by range
-// boundaries leaves an (m, l, O) partial per part (two slots per CTA), and the
-// part that finishes last merges them.
+// of prefix lengths.  A pair that lies inside one range is finished in place;
+// a pair cut by range boundaries leaves an (m, l, O) partial per part (two
+// slots per CTA), and the part that finishes last merges them.  In stream-K
+// order that is usually a CTA's last segment, whose partner part finished long
+// before: when every other part has already left its partial, the last part
+// merges straight from its TMEM accumulators (one acquire load of the pair's
+// counter decides) instead of writing, handing over and re-reading its own.
 //
 // Per CTA (12 warps, so each SM sub-partition hosts one helper warp and two
 // softmax warps):
@@ -58,6 +61,7 @@ constexpr int kD = 128;             // head dimension
 constexpr int BN = 64;              // keys per tile
 constexpr float kRescaleLog2 = 8.f; // O is rescaled only when the row maximum grows by more than this
 constexpr int kMaxB = 1024;
+constexpr int kEarlyParts = 4;      // other parts a split pair may have for the direct merge
 
 template <int MT>
 struct Cfg {
@@ -93,6 +97,7 @@ struct Bars {
   uint64_t mrg_in, mrg_go;  // hand-off of a pair shared by several CTAs
   uint32_t tmem;
   int abort, mrg_last;
+  int mrg_early;  // MT == 1: every other part of this split pair has already left its partial
   float2 ml_x[2][2][128];  // each warpgroup's (m, l) per row, by segment parity (MT == 1)
   int Ls[kMaxB];
   int pref[kMaxB + 1];  // first tile of sequence b in the global tile order
@@ -559,8 +564,24 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         m_run = -INFINITY;
         l_run = 0.f;
       }
+      // the CTAs that own parts of a split pair: CTA c owns
+      // [total*c/grid, total*(c+1)/grid), so the owner of tile t is ceil((t+1)*grid/total) - 1
+      const long long p_total = bars->pref[a.B];
+      const int p_grid = (int)gridDim.x;
+      const long long p_first = bars->pref[sg.b] + (long long)(sg.g * a.HG + sg.hg) * tiles_per_pair(sg.Lb, N);
+      const long long p_last = p_first + tiles_per_pair(sg.Lb, N) - 1;
+      const int pc0 = (int)(((p_first + 1) * p_grid + p_total - 1) / p_total - 1);
+      const int pc1 = (int)(((p_last + 1) * p_grid + p_total - 1) / p_total - 1);
       float2 other = make_float2(-INFINITY, 0.f);
       if (MT == 1) {
+        // A split pair whose other parts have all left their partials (at most
+        // kEarlyParts of them): this part merges straight from its accumulators
+        // instead of writing a partial, handing over and reading it back.
+        if (threadIdx.x == 128 && !sg.complete) {
+          int seen;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(a.cnt + sg.pair) : "memory");
+          bars->mrg_early = pc1 - pc0 <= kEarlyParts && seen == pc1 - pc0;
+        }
         // both warpgroups publish their (m, l); each then finishes half of the d columns
         bars->ml_x[sc & 1][grp][r] = make_float2(m_run, l_run);
         mbar_arrive(&bars->ml_ready);
@@ -577,7 +598,77 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       const float l = l_run * wa + other.y * wb;
       constexpr int COLS = MT == 1 ? kD / 2 : kD;  // columns this unit finishes
       const int col0 = MT == 1 ? grp * COLS : 0;
-      if (warp_active) {
+      const bool early = MT == 1 && !sg.complete && bars->mrg_early;
+      const int slot_pc0 = pc0 * 2 + (range_start(p_total, pc0, p_grid) < p_first ? 1 : 0);
+      auto part_row = [&](int c) {
+        const int slot = c == pc0 ? slot_pc0 : c * 2;
+        return ((long long)slot * MT + mt) * N + r;
+      };
+      if (early) {
+        if (warp_active) {
+          __threadfence();
+          // the other parts' (m, l) and rows, this part's (M, l) from above
+          float wk[kEarlyParts];
+          long long rk[kEarlyParts];
+          int nk = 0;
+          float Mx = M;
+#pragma unroll 1
+          for (int c = pc0; c <= pc1; ++c) {
+            if (c == (int)blockIdx.x) continue;
+            rk[nk] = part_row(c);
+            const float2 ml = row_valid ? __ldcg(&a.part_ml[rk[nk]]) : make_float2(-INFINITY, 0.f);
+            wk[nk] = ml.x;  // the maximum for now, the weight below
+            Mx = fmaxf(Mx, ml.x);
+            ++nk;
+          }
+          const float wown = M == -INFINITY ? 0.f : ex2(M - Mx);
+          float den = l * wown;
+#pragma unroll 1
+          for (int k = 0; k < nk; ++k) {
+            const float w = wk[k] == -INFINITY ? 0.f : ex2(wk[k] - Mx);
+            den += (row_valid ? __ldcg(&a.part_ml[rk[k]]).y : 0.f) * w;
+            wk[k] = w;
+          }
+          const float inv = den > 0.f ? 1.f / den : 0.f;  // > 0 for a valid row: every node sees itself
+          const float w0 = (grp == 0 ? wa : wb) * wown, w1 = (grp == 0 ? wb : wa) * wown;
+          float *dst = a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD;
+#pragma unroll 1
+          for (int c0 = col0; c0 < col0 + COLS; c0 += 32) {
+            float oa[32], ob[32];
+            tmem_ld32(tmem + lane_off + C::o_col(0) + c0, oa);
+            tmem_ld32(tmem + lane_off + C::o_col(1) + c0, ob);
+            if (c0 + 32 == col0 + COLS) {
+              // the last read of the accumulators: the next segment's PV may overwrite them
+              tc_fence_before();
+              mbar_arrive(&bars->o_empty);
+            }
+            if (row_valid) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) oa[c] = (w0 != 0.f ? oa[c] * w0 : 0.f) + (w1 != 0.f ? ob[c] * w1 : 0.f);
+#pragma unroll 1
+              for (int k = 0; k < nk; ++k) {
+                const float4 *src = reinterpret_cast<const float4 *>(a.part_o + rk[k] * kD + c0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float4 v = __ldcg(src + i);
+                  oa[4 * i] += v.x * wk[k];
+                  oa[4 * i + 1] += v.y * wk[k];
+                  oa[4 * i + 2] += v.z * wk[k];
+                  oa[4 * i + 3] += v.w * wk[k];
+                }
+              }
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4 *>(dst + c + c0) =
+                    make_float4(oa[c] * inv, oa[c + 1] * inv, oa[c + 2] * inv, oa[c + 3] * inv);
+            }
+          }
+          if (threadIdx.x == 128) a.cnt[sg.pair] = 0;  // the workspace is left zeroed
+        } else {
+          tc_fence_before();
+          mbar_arrive(&bars->o_empty);
+        }
+      } else if (warp_active) {
         const int slot = blockIdx.x * 2 + (sg.first_of_cta ? 0 : 1);
         const long long prow_idx = ((long long)slot * MT + mt) * N + r;
         const float scale_out = sg.complete ? (row_valid && l > 0.f ? 1.f / l : 0.f) : 1.f;
@@ -612,17 +703,12 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         tc_fence_before();
         mbar_arrive(&bars->o_empty);
       }
-      if (!sg.complete) {
+      if (!sg.complete && !early) {
         // A pair shared by several CTAs (cut by range boundaries): each part
         // leaves its partial in a slot and counts itself; the last part to
         // finish merges them all and resets the counter.
-        const long long total = bars->pref[a.B];
-        const int grid = (int)gridDim.x;
-        const int tpp = tiles_per_pair(sg.Lb, N);
-        const long long first = bars->pref[sg.b] + (long long)(sg.g * a.HG + sg.hg) * tpp, last = first + tpp - 1;
-        // CTA c owns [total*c/grid, total*(c+1)/grid): the owner of tile t is ceil((t+1)*grid/total) - 1
-        const int c0 = (int)(((first + 1) * grid + total - 1) / total - 1);
-        const int c1 = (int)(((last + 1) * grid + total - 1) / total - 1);
+        const long long total = p_total, first = p_first;
+        const int grid = p_grid, c0 = pc0, c1 = pc1;
         __threadfence();
         mbar_arrive(&bars->mrg_in);
         if (threadIdx.x == 128) {
