@@ -234,7 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Final merge: one warp per row reduces n_lists lists of KMAX keys.
+// Final merge: one warp per row reduces n_lists lists of KMAX keys.  A lane
+// takes every 32nd list; each list arrives with 16-byte loads issued before
+// any key is used, and since a list is sorted, its first key that cannot
+// enter ends it.
 template <int KMAX>
 __global__ void __launch_bounds__(128) merge_lists_kernel(const unsigned long long *part, long long rows, int n_lists,
                                                           int K, int32_t *ids, float *vals) {
@@ -243,13 +246,25 @@ __global__ void __launch_bounds__(128) merge_lists_kernel(const unsigned long lo
   if (row >= rows) return;
   TopList<KMAX> L;
   L.init();
-  for (int t = lane; t < n_lists; t += 32) {
-    const unsigned long long *src = part + (row * n_lists + t) * KMAX;
-    for (int j = 0; j < KMAX; ++j) {
-      const unsigned long long key = src[j];
-      if (key == 0ull) break;
-      list_insert<KMAX>(L.k, key);
+  constexpr int kLists = KMAX <= 8 ? 4 : (KMAX <= 16 ? 2 : 1);  // lists a lane holds in registers at once
+  for (int t0 = lane; t0 < n_lists; t0 += 32 * kLists) {
+    ulonglong2 buf[kLists][KMAX / 2];
+#pragma unroll
+    for (int q = 0; q < kLists; ++q) {
+      const int t = t0 + 32 * q;
+      const ulonglong2 *src = reinterpret_cast<const ulonglong2 *>(part + (row * n_lists + t) * KMAX);
+#pragma unroll
+      for (int j = 0; j < KMAX / 2; ++j) buf[q][j] = t < n_lists ? __ldcs(src + j) : make_ulonglong2(0ull, 0ull);
     }
+#pragma unroll
+    for (int q = 0; q < kLists; ++q)
+#pragma unroll
+      for (int j = 0; j < KMAX / 2; ++j) {
+        if (buf[q][j].x <= L.k[KMAX - 1]) break;  // sorted: nothing further in this list enters
+        list_insert<KMAX>(L.k, buf[q][j].x);
+        if (buf[q][j].y <= L.k[KMAX - 1]) break;
+        list_insert<KMAX>(L.k, buf[q][j].y);
+      }
   }
   const unsigned long long mine = warp_merge<KMAX>(L, lane);
   if (lane < K) {
