@@ -42,11 +42,13 @@
 //               partial.
 // TMEM holds two O accumulators (128 columns each) and four S/P buffers of
 // 64 columns; a buffer is reused by the QK product four tiles later, once the
-// PV product that read its P has completed.  With MT = 1 two softmax
-// warpgroups take alternate tiles into their own accumulators (combined at
-// the end of a segment); with MT = 2 the two query heads sharing one KV head
-// are processed together (grouped-query attention), one warpgroup and one
-// accumulator per head, so every K/V tile feeds 256 query rows.
+// PV product that read its P has completed.  The two softmax warpgroups take
+// alternate tiles into their own accumulators (combined at the end of a
+// segment).  The kernel is written for MT query heads per pair; it launches
+// with MT = 1 (grouped-query heads too, one pair per query head), since two
+// heads per K/V tile (MT = 2: one warpgroup and one accumulator per head, 256
+// query rows per tile, half the K/V reads) measured slower on grouped-query
+// shapes, which are bound by the tensor pipe and the exponentials.
 //
 // Every wait is bounded in time; a wait that gives up sets TR_DEV_TIMEOUT and
 // raises a block-wide abort flag; the roles drain their in-flight copies and
@@ -85,7 +87,6 @@ struct Cfg {
   __host__ __device__ static constexpr uint32_t s_col(int buf, int m) { return (uint32_t)(2 * kD + (buf * MT + m) * BN); }
 };
 static_assert(Cfg<1>::s_col(Cfg<1>::NSB - 1, 0) + BN <= Cfg<1>::TMEM_COLS, "TMEM budget");
-static_assert(Cfg<2>::s_col(Cfg<2>::NSB - 1, 1) + BN <= Cfg<2>::TMEM_COLS, "TMEM budget");
 
 template <int MT>
 struct Bars {
@@ -803,7 +804,11 @@ int launch_grid(const Plan &p, int B, int Hkv, int cap, int N) {
 Plan make_plan(int B, int Hq, int Hkv, int N) {
   Plan p;
   p.G = Hq / Hkv;
-  p.MT = p.G % 2 == 0 ? 2 : 1;
+  // one query head per pair, also for grouped-query heads: two heads per
+  // K/V tile (MT = 2) halve the K/V reads but measured slower on the
+  // grouped-query shapes tried (32 query / 8 KV heads, prefixes 4096 and
+  // 32768), which are bound by the tensor pipe and the exponentials, not HBM
+  p.MT = 1;
   p.HG = p.G / p.MT;
   p.pairs = B * Hkv * p.HG;
   p.grid = tr_sm_count();
@@ -879,24 +884,15 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = (cudaStream_t)stream;
   const int grid = launch_grid(p, B, Hkv, cap, N);
-  static bool attr_set[2][64];
+  static bool attr_set[1][64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (p.MT == 1) {
-    if (dev >= 0 && dev < 64 && !attr_set[0][dev]) {
-      TR_TRY_CUDA(cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_bytes<1>()));
-      attr_set[0][dev] = true;
-    }
-    attn_tc_kernel<1><<<grid, Cfg<1>::THREADS, smem_bytes<1>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
-  } else {
-    if (dev >= 0 && dev < 64 && !attr_set[1][dev]) {
-      TR_TRY_CUDA(cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_bytes<2>()));
-      attr_set[1][dev] = true;
-    }
-    attn_tc_kernel<2><<<grid, Cfg<2>::THREADS, smem_bytes<2>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
+  if (dev >= 0 && dev < 64 && !attr_set[0][dev]) {
+    TR_TRY_CUDA(cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes<1>()));
+    attr_set[0][dev] = true;
   }
+  attn_tc_kernel<1><<<grid, Cfg<1>::THREADS, smem_bytes<1>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
   TR_LAUNCH_CHECK();
   return TR_OK;
 }
