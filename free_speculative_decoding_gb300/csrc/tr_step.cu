@@ -111,12 +111,26 @@ __device__ void block_accept(const TreeDev &tree, AcceptSmem &s) {
   __syncthreads();
 }
 
-__device__ void load_tree_state(const TreeDev &tree, const int32_t *tok, const int32_t *ids, int K, AcceptSmem &s) {
+// With ids_s, every node's whole top-K row is loaded into it in the same round
+// trip as the top-1 IDs.
+__device__ void load_tree_state(const TreeDev &tree, const int32_t *tok, const int32_t *ids, int K, AcceptSmem &s,
+                                int32_t *ids_s = nullptr) {
   const int n = threadIdx.x;
   if (n < 2) s.nomatch[n] = 0ull;
   if (n < tree.N) {
     s.tok[n] = tok[n];
-    s.top1[n] = ids[(long long)n * K];
+    if (ids_s) {
+      int32_t v[TR_MAX_K];
+#pragma unroll
+      for (int k = 0; k < TR_MAX_K; ++k)
+        if (k < K) v[k] = ids[(long long)n * K + k];
+#pragma unroll
+      for (int k = 0; k < TR_MAX_K; ++k)
+        if (k < K) ids_s[n * K + k] = v[k];
+      s.top1[n] = v[0];
+    } else {
+      s.top1[n] = ids[(long long)n * K];
+    }
   }
   __syncthreads();
 }
@@ -337,13 +351,13 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(FinishArgs a, const __
       wt.node[h] = -1;
     }
   }
-  load_tree_state(tree, a.tree_tok + (long long)b * N, ids_b, K, s);
+  load_tree_state(tree, a.tree_tok + (long long)b * N, ids_b, K, s, part == 0 ? ids_s : nullptr);
   block_accept(tree, s);
   const int acc = s.acc_len;
   if (part == 0) {
     write_accept_outputs(tree, s, b, a.acc_len, a.path, a.committed, nullptr);
     T *Mb = (T *)a.M + (long long)b * a.V * K;
-    // writers: every node, or the accepted path; their top-K rows into shared memory
+    // writers: every node, or the accepted path (all top-K rows are in ids_s)
     bool w = false;
     int t = 0;
     if (n < N) {
@@ -353,10 +367,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(FinishArgs a, const __
         tr_flag(a.status, TR_DEV_BAD_TOKEN);
         w = false;
       }
-      if (w) {
-        for (int k = 0; k < K; ++k) ids_s[n * K + k] = ids_b[(long long)n * K + k];
-        wt.insert(t, n);
-      }
+      if (w) wt.insert(t, n);
     }
     __syncthreads();
     // last writer in BFS order stores its row

@@ -270,8 +270,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
       for (int j = 0; j < kVecs; ++j) vmx[j] = j * 32 + lane < nvec ? Elem<T>::vmax(sv[j * 32 + lane]) : NAN;
     }
+    // NaN when the lane holds no element of the step (a short last step of a
+    // row, or everything handed over), so that such a lane never takes part
     auto lane_max = [&]() {
-      float m = fmaxf(-INFINITY, tv);
+      float m = tv;
 #pragma unroll
       for (int j = 0; j < kVecs; ++j) m = fmaxf(m, vmx[j]);
       return m;
@@ -280,8 +282,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     // An element enters only above the floor f: the K-th best value held,
     // when there is one (the held keys all come from earlier steps, with
     // lower IDs, so only a strictly larger value can enter); else the K-th
-    // largest lane maximum, which K elements of this step reach.
-    float f = have_k ? thr : warp_kth(lm, K, lane);
+    // largest lane maximum, which K elements of this step reach (-inf when
+    // fewer than K lanes hold an element).
+    float f = have_k ? thr : warp_kth(isnan(lm) ? -INFINITY : lm, K, lane);
     bool strict = have_k;
     // Each pass takes every lane's largest remaining element above the floor
     // (the lowest ID among equal values), inserts those keys into the held

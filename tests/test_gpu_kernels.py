@@ -173,6 +173,33 @@ def test_topk_strided_rows_and_empty(tr, ld):
     tr.tr_topk(e, 4, torch.zeros(0, 4, dtype=torch.int32, device="cuda"), None, None)
 
 
+@pytest.mark.parametrize("V,ld,rows,K,dtype", [
+    (24, 24, 40, 8, torch.float32),          # one step: 6 of 32 lanes hold an element
+    (16, 16, 9, 16, torch.float32),          # V == K: 4 lanes
+    (6152, 6152, 700, 8, torch.float32),     # a row's last step: 2 vectors
+    (8208, 8208, 500, 16, torch.bfloat16),   # a row's last step: 2 vectors of 8
+    (4099, 4100, 600, 8, torch.float32),     # a row's last step: 3 loose elements, no whole vector
+])
+def test_topk_short_last_steps(tr, V, ld, rows, K, dtype):
+    # 16-byte aligned rows whose last 8 KB step gives fewer than K lanes an
+    # element, and enough rows that warp ranges start on such steps: a lane
+    # without an element must never take part, even when the floor is -inf
+    g = torch.Generator().manual_seed(V + rows)
+    x = torch.round(torch.randn(rows, ld, generator=g) * 12) / 4   # ties
+    x[:, V:] = 100.0                         # beyond V: never a candidate
+    x = x.to(dtype)
+    ids_ref, vals_ref = oracle.topk_rows(x[:, :V].float().numpy(), K)
+    ids = torch.zeros(rows, K, dtype=torch.int32, device="cuda")
+    vals = torch.zeros(rows, K, dtype=torch.float32, device="cuda")
+    ws = tr.workspace(tr.tr_topk_workspace_bytes(rows, V, K))
+    xd = x.cuda()
+    for _ in range(2):
+        tr.tr_topk(xd, K, ids, vals, ws, V=V)
+        assert np.array_equal(ids.cpu().numpy(), ids_ref)
+        assert np.array_equal(vals.cpu().numpy(), vals_ref.astype(np.float32))
+    _status_ok(tr)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_topk_all_equal_and_few_values(tr, dtype):
     # every element ties: far more candidates than the shared-memory ranking
