@@ -335,6 +335,9 @@ def run_gpu(args, rank, world):
             tev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(max(8, nslot))]
             torch.cuda.synchronize()
+            # the same device-side spin: every launch is queued before the
+            # first start event, so each interval holds the kernel alone
+            torch.cuda._sleep(2 * PRIME_CYCLES)
             for j, (e0, e1) in enumerate(tev):
                 e0.record(stream)
                 tr.tr_topk(bufs["logits"][j % nslot], w.K, ids, vals, ws)
