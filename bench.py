@@ -57,6 +57,14 @@ def load_peaks():
     return PEAK_FALLBACK, "fallback"
 
 
+def config_of(args, wl, world):
+    """The workload as both arms name it in their JSON line."""
+    return {"workload": args.workload, "B": wl.B, "V": wl.V, "K": wl.K, "tree": wl.tree, "tree_nodes": wl.N,
+            "tree_depth": wl.depth(), "prefix": list(wl.prefix), "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+            "parallelism": "replicas (dp%d, no collective)" % world,
+            "l2": "per-step inputs larger than L2 (fresh logits + KV cache)"}
+
+
 def src_sha(*names):
     h = hashlib.sha256()
     for name in names:
@@ -523,7 +531,7 @@ def main():
         line = {"impl": "reference", "metric": metric, "value": rate, "unit": unit, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / rate, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention / exact compare", "data": "synthetic",
-                "config": {"workload": args.workload},
+                "config": config_of(args, w, world), "timed": "the oracle on a bounded sample of the workload",
                 "cpu_baseline": {"value": rate, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
                                  "sample": "%d sequence-steps of sequence 0 (%.1f s), scaled to %d sequences"
                                            % (n, spent, w.B)},
@@ -575,12 +583,7 @@ def main():
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 attention (fp32 accumulate), %s logits, int64/int32 state" % wl.logits,
         "data": "synthetic (seeded splitmix64 target; see DESIGN.md)",
-        "config": {"workload": args.workload, "B": wl.B, "V": wl.V, "K": wl.K, "tree": wl.tree, "tree_nodes": N,
-                   "tree_depth": wl.depth(),
-                   "prefix": list(wl.prefix), "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
-                   "parallelism": "replicas (dp%d, no collective)" % world,
-                   "l2": "per-step inputs larger than L2 (fresh logits + KV cache)",
-                   "timed": "record-then-replay: hot-path kernels only"},
+        "config": config_of(args, wl, world), "timed": "record-then-replay: hot-path kernels only",
         "tree_tokens_per_s": value * wl.B * N,
         "committed_tokens_per_s": world * res["committed"] / (res["total_ms"] * 1e-3),
         "mat": res["committed"] / (K * wl.B),
