@@ -62,7 +62,10 @@ def config_of(args, wl, world):
     return {"workload": args.workload, "B": wl.B, "V": wl.V, "K": wl.K, "tree": wl.tree, "tree_nodes": wl.N,
             "tree_depth": wl.depth(), "prefix": list(wl.prefix), "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
             "parallelism": "replicas (dp%d, no collective)" % world,
-            "l2": "per-step inputs larger than L2 (fresh logits + KV cache)"}
+            "l2": ("every step reads its own recorded hidden rows; the weight (V x D bf16) is larger than L2"
+                   if wl.logits == "lmhead" else
+                   "every step reads its own recorded logits and Q/K/V (all steps together far larger than L2) "
+                   "and the KV cache")}
 
 
 def src_sha(*names):
