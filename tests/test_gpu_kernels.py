@@ -136,6 +136,8 @@ def test_worked_example_on_gpu(tr, golden_dir):
 @pytest.mark.parametrize("V,rows,K,dtype", [
     (32000, 80, 8, "f32"), (32000, 1280, 8, "f32"), (128256, 64, 8, "bf16"), (37, 5, 3, "f32"),
     (8193, 33, 16, "bf16"), (16387, 7, 32, "f32"), (100, 3, 1, "bf16"), (300001, 2, 8, "f32"),
+    # aligned rows (the warp-streaming kernel) with 1-, 16- and 32-key lists
+    (32000, 40, 1, "f32"), (32000, 50, 32, "f32"), (128256, 16, 32, "bf16"), (20480, 70, 16, "bf16"),
 ])
 def test_topk_matches_oracle(tr, V, rows, K, dtype):
     g = torch.Generator().manual_seed(V + rows + K)
@@ -380,14 +382,17 @@ def test_attention_matches_oracle(tr, tree_name, B, Hq, Hkv, lens):
 # fused LM head + top-K
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("rows,D,V,sample", [
-    (200, 1024, 5000, None),      # one row tile, both halves partly past the rows
-    (600, 512, 9001, None),       # three row tiles, a ragged last column tile
-    (2560, 4096, 32000, 97),      # the full LM-head workload, every 97th row checked
+@pytest.mark.parametrize("rows,D,V,sample,K", [
+    (200, 1024, 5000, None, 8),      # one row tile, both halves partly past the rows
+    (600, 512, 9001, None, 8),       # three row tiles, a ragged last column tile
+    (2560, 4096, 32000, 97, 8),      # the full LM-head workload, every 97th row checked
+    (300, 512, 5000, None, 16),      # 16-key lists
+    (300, 512, 4097, None, 32),      # 32-key lists; the last column tile holds one column
+    (130, 512, 777, None, 3),        # K below the list size
+    (129, 512, 600, None, 1),        # top-1 only
 ])
-def test_lmhead_exact_grid_workload(tr, rows, D, V, sample):
+def test_lmhead_exact_grid_workload(tr, rows, D, V, sample, K):
     w = synth.WORKLOADS["lmhead"]
-    K = 8
     tok = np.arange(rows) * 37 % V
     H = synth.lm_hidden_rows(w.seed, 0, np.arange(rows), tok, D)
     Wt = synth.lm_weight_rows(w.seed, V, D)
