@@ -220,6 +220,15 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     bars->abort = 0;
     fence_mbar_init();
   }
+  // A TMA box shorter than a 64-key tile (a tree or cache tensor of fewer
+  // than 64 rows: tiny batches) leaves the tile's last rows unwritten.  Their
+  // keys get weight zero, but zero times a NaN left in shared memory would
+  // still reach O, so the V ring starts zeroed then.
+  if (a.t_rows < BN || a.c_rows < BN) {
+    uint4 *vr = reinterpret_cast<uint4 *>(smem + C::OFF_V);
+    for (int i = threadIdx.x; i < VS * C::KV_TILE / 16; i += blockDim.x) vr[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();  // the zeros come before the ring's first copies and products
+  }
   for (int b = threadIdx.x; b < a.B; b += blockDim.x) {
     int Lb = a.L[b];
     if (Lb < 0 || Lb > a.cap) {

@@ -346,17 +346,21 @@ def test_bad_token_and_full_cache_are_flagged(tr):
 # tree attention
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("tree_name,B,Hq,Hkv,lens", [
-    ("T80", 2, 8, 8, [0, 1500]),          # empty prefix; several chunks with a ragged tail
-    ("T128", 2, 8, 2, [1023, 2049]),      # grouped-query heads, chunk-boundary lengths
-    ("T80", 1, 4, 4, [4096]),
+@pytest.mark.parametrize("tree_name,B,Hq,Hkv,lens,cap", [
+    ("T80", 2, 8, 8, [0, 1500], None),          # empty prefix; several chunks with a ragged tail
+    ("T128", 2, 8, 2, [1023, 2049], None),      # grouped-query heads, chunk-boundary lengths
+    ("T80", 1, 4, 4, [4096], None),
+    # fewer than 64 tree rows in the whole batch (TMA boxes shorter than a tile); 8 query heads on one KV head
+    ([1, 1, 0], 3, 8, 1, [5, 64, 0], None),
+    ([0], 2, 4, 4, [0, 70], None),              # the root alone
+    ([2, 0, 0], 1, 2, 1, [33], 40),             # a cache tensor of 40 rows
 ])
-def test_attention_matches_oracle(tr, tree_name, B, Hq, Hkv, lens):
-    counts = synth.TREES[tree_name]
+def test_attention_matches_oracle(tr, tree_name, B, Hq, Hkv, lens, cap):
+    counts = synth.TREES[tree_name] if isinstance(tree_name, str) else tree_name
     tree = tr.Tree(counts, 8)
     plan = oracle.TreePlan(counts, 8)
     N, d = plan.N, 128
-    cap = max(lens) + 16
+    cap = cap or max(lens) + 16
     g = torch.Generator().manual_seed(B * 100 + Hq)
     q = torch.randn(B, N, Hq, d, generator=g).to(torch.bfloat16)
     kt = torch.randn(B, N, Hkv, d, generator=g).to(torch.bfloat16)
