@@ -98,3 +98,39 @@ def test_workspace_sizes(lib):
     t = tr.Tree(synth.TREE_T80, 8)
     assert lib.tr_verify_attn_workspace_bytes(16, 32, 32, 128, 5888, t.handle) > 0
     assert lib.tr_kv_commit_workspace_bytes(16) >= 64
+
+
+def test_step_and_noalloc_validation_before_any_launch(lib):
+    # every case is refused on the host, before the device is touched
+    import free_speculative_decoding_gb300 as tr
+    t = tr.Tree(synth.TREE_T80, 8)
+    p = 16  # an address that is never dereferenced
+
+    def args(**kw):
+        a = tr.tr_step_args(B=2, V=1000, K=8, tree=t.handle, M=p, mtype=tr.TR_I64, logits=p, ltype=tr.TR_F32,
+                            ld=1000, tree_tok=p, ids=p, acc_len=p, path=p, committed=p, root=p, L=p,
+                            mode=tr.TR_UPD_ALL)
+        a.ws, a.ws_bytes = p, 1 << 40
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return a
+
+    step = lambda a: lib.tr_step(ctypes.byref(a), None)
+    assert lib.tr_step(None, None) == tr.TR_E_INVAL
+    assert step(args(K=4)) == tr.TR_E_INVAL                       # K differs from the tree's
+    assert step(args(mtype=9)) == tr.TR_E_INVAL
+    assert step(args(mode=9)) == tr.TR_E_INVAL
+    assert step(args(logits=None)) == tr.TR_E_INVAL               # neither logits nor H and Wt
+    assert step(args(M=None)) == tr.TR_E_INVAL
+    assert step(args(Kt=p, Vt=None, Kc=p, Vc=p, cap=64, Hkv=2, d=128)) == tr.TR_E_INVAL   # Kt without Vt
+    assert step(args(Kt=p, Vt=p, Kc=p + 8, Vc=p, cap=64, Hkv=2, d=128)) == tr.TR_E_INVAL  # misaligned cache
+    assert step(args(Kt=p, Vt=p, Kc=p, Vc=p, cap=64, Hkv=2, d=100)) == tr.TR_E_INVAL      # d % 8
+    a = args()
+    a.ws_bytes = 0
+    assert step(a) == tr.TR_E_INVAL                                  # workspace too small
+    assert lib.tr_step_workspace_bytes(ctypes.byref(args())) > 0
+    # the allocation-free top-K refuses what its static scratch cannot hold
+    assert lib.tr_topk_noalloc(p, tr.TR_F32, 4, 10, 10, 11, p, None, None) == tr.TR_E_INVAL          # K > V
+    assert lib.tr_topk_noalloc(p, tr.TR_F32, 70000, 10, 10, 3, p, None, None) == tr.TR_E_UNSUPPORTED  # rows
+    assert lib.tr_topk_noalloc(p, tr.TR_BF16, 60000, 128256, 128256, 8, p, None,
+                               None) == tr.TR_E_UNSUPPORTED                                           # scratch
