@@ -497,7 +497,32 @@ def oracle_rate(w, budget_s, max_seq_steps=None):
 
 
 def cpu_cores():
-    return os.cpu_count() or 1
+    """The host cores this process may run on (numpy's BLAS may use them all)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_rate_one_core(args, budget_s, max_seq_steps=None):
+    """oracle_rate on one core: a child process pinned to one CPU with one BLAS
+    thread.  Returns a cpu_baseline-style dict, or None if the child failed."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               RANK="0", WORLD_SIZE="1")
+    code = ("import os, sys, json, types\n"
+            "os.sched_setaffinity(0, {min(os.sched_getaffinity(0))})\n"
+            "sys.path.insert(0, %r)\n"
+            "import bench\n"
+            "w = bench.workload_of(types.SimpleNamespace(workload=%r, tree=%r))\n"
+            "print(json.dumps(bench.oracle_rate(w, %r, %r)))\n"
+            % (ROOT, args.workload, args.tree, float(budget_s), max_seq_steps))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+        rate, n, spent = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return {"value": rate, "cores": 1,
+            "sample": "%d sequence-steps of sequence 0 (%.1f s) on one pinned core, one BLAS thread" % (n, spent)}
 
 
 # ----------------------------------------------------------------------------
@@ -539,6 +564,11 @@ def main():
                                  "sample": "%d sequence-steps of sequence 0 (%.1f s), scaled to %d sequences"
                                            % (n, spent, w.B)},
                 "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        if args.workload == "tiny":
+            # the latency-bound single-sequence loop: also its one-core oracle rate
+            one = oracle_rate_one_core(args, per_step * args.steps, args.steps)
+            if one:
+                line["cpu_baseline"]["one_core"] = one
         print(json.dumps(line))
         return
 
@@ -617,6 +647,10 @@ def main():
     line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
                             "sample": "%d sequence-steps of sequence 0 (%.1f s of oracle time), scaled to %d "
                                       "sequences; BLAS calls may use all cores" % (n, spent, wl.B)}
+    if args.workload == "tiny" and world == 1:
+        one = oracle_rate_one_core(args, args.cpu_budget)
+        if one:
+            line["cpu_baseline"]["one_core"] = one
     print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist

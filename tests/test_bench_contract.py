@@ -41,6 +41,9 @@ def test_reference_line(workload, tree):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == d["unit"] and cb["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # the single-sequence loop also reports the oracle on one pinned core
+    one = cb["one_core"]
+    assert one["cores"] == 1 and one["value"] > 0
     # the same workload description the GPU arm prints
     ns = types.SimpleNamespace(workload=workload, tree=tree)
     w = bench.workload_of(ns)
