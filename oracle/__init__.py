@@ -25,8 +25,8 @@ Sources, cited by page title and section:
   token, tree attention where each node sees only its ancestors, and the
   expected tokens per pass of an i.i.d. linear draft.
 
-Readings where the pages are silent or ambiguous are listed in the design doc
-and repeated next to the function they affect.
+Where the pages are silent or ambiguous, the reading taken is stated next to
+the function it affects.
 
 Every function here is pinned by a ``-m "not gpu"`` test against something
 other than itself (a worked example, brute force, a closed form or a special
@@ -36,12 +36,13 @@ from .tree import TreePlan
 from .tr import (
     INIT_ZERO, INIT_RANDOM, INIT_INHERIT, UPD_ALL, UPD_ACCEPTED,
     init_matrix, retrieve, tree_attention, topk, topk_rows, accept, update,
-    kv_commit, lmhead_logits, mix64_stream,
+    kv_commit, lmhead_logits, mix64_stream, softmax_stats, target_probs, accept_sampled,
 )
 from .loop import TRState, tr_loop, greedy_decode
 
 __all__ = [
     "TreePlan", "INIT_ZERO", "INIT_RANDOM", "INIT_INHERIT", "UPD_ALL", "UPD_ACCEPTED",
     "init_matrix", "retrieve", "tree_attention", "topk", "topk_rows", "accept", "update",
-    "kv_commit", "lmhead_logits", "mix64_stream", "TRState", "tr_loop", "greedy_decode",
+    "kv_commit", "lmhead_logits", "mix64_stream", "softmax_stats", "target_probs", "accept_sampled",
+    "TRState", "tr_loop", "greedy_decode",
 ]

@@ -14,7 +14,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .tr import UPD_ALL, accept, kv_commit, retrieve, topk_rows, tree_attention, update
+from .tr import UPD_ALL, accept, accept_sampled, kv_commit, retrieve, topk_rows, tree_attention, update
 
 
 @dataclass
@@ -29,7 +29,7 @@ class TRState:
 
 
 def tr_loop(plan, states, target, steps, K, mode=UPD_ALL, qkv=None, scale=None,
-            on_step=None, seqs=None):
+            on_step=None, seqs=None, temperature=None, uniforms=None):
     """Run ``steps`` Token Recycling steps over the sequences in ``states``.
 
     ``qkv(step)`` (optional) returns (q [B,N,Hq,d], kt [B,N,Hkv,d],
@@ -37,6 +37,9 @@ def tr_loop(plan, states, target, steps, K, mode=UPD_ALL, qkv=None, scale=None,
     attention and commits the accepted K/V rows to each cache.  ``seqs``
     maps state index to the sequence index handed to the target.
     ``on_step(step, b, rec)`` receives every sequence's record.
+    With ``temperature`` the acceptance samples (accept_sampled) with the
+    uniforms ``uniforms(step, b)`` [N, K+1]; the matrix update is the same
+    top-K of every node either way.
     """
     seqs = list(range(len(states))) if seqs is None else list(seqs)
     depth = np.asarray(plan.depth)
@@ -53,7 +56,11 @@ def tr_loop(plan, states, target, steps, K, mode=UPD_ALL, qkv=None, scale=None,
             rows = target(b, st.L + depth, tok)
             ids, vals = topk_rows(rows, K)
             rec["ids"], rec["vals"] = ids, vals
-            acc_len, path, committed, bonus = accept(plan, tok, ids[:, 0])
+            if temperature is None:
+                acc_len, path, committed, bonus = accept(plan, tok, ids[:, 0])
+            else:
+                acc_len, path, committed, bonus, rec["margin"] = accept_sampled(
+                    plan, tok, rows, temperature, uniforms(s, b))
             update(st.M, tok, ids, plan, mode, path)
             if q is not None:
                 st.L = kv_commit(st.kc, st.vc, kt[i], vt[i], st.L, path)

@@ -155,6 +155,84 @@ def accept(plan, tok, top1):
     return plan.depth[best], path, committed, bonus
 
 
+def softmax_stats(row, T):
+    """(max, Z) of one row at temperature T, in fp64: Z = sum_v exp((x_v - max) / T).
+
+    The target's distribution at a node is p = softmax(x / T), so
+    p(v) = exp((x_v - max) / T) / Z (the speculative-decoding lesson's
+    sampling setting; T = 1 is plain sampling, T -> 0 greedy decoding)."""
+    x = np.asarray(row, dtype=np.float64)
+    m = x.max()
+    return m, float(np.exp((x - m) / T).sum())
+
+
+def target_probs(row, T):
+    """The target's sampling distribution softmax(row / T) at one node, fp64."""
+    m, Z = softmax_stats(row, T)
+    return np.exp((np.asarray(row, dtype=np.float64) - m) / T) / Z
+
+
+def accept_sampled(plan, tok, logits, T, U):
+    """Acceptance under sampling at temperature T: the path taken, the tokens
+    committed, and how close each decision came to its threshold.
+
+    Speculative-decoding lesson, the acceptance rule: walking the draft, a
+    drafted token x is accepted with probability min(1, p(x) / q(x)); on the
+    first rejection the token is resampled from norm(max(0, p - q)), and when
+    every drafted token is accepted one more token is sampled from p (the
+    bonus).  The output is then distributed exactly as sampling from p alone.
+    hyper.ai summary, "Experiment": Token Recycling stays effective under
+    sampling, but the pages give no rule for its tree.  The reading taken
+    here: Token Recycling's draft is deterministic -- the child tokens are
+    fixed by the matrix -- so each child's draft distribution q is one-hot on
+    its token, and the rule is applied to a node's children in rank order:
+    child x is accepted with probability min(1, r(x) / 1) = r(x) under the
+    current residual r (at first r = p); when it is rejected,
+    r <- norm(max(0, r - onehot(x))), which zeroes r(x) and renormalises, and
+    the next child is tried.  An accepted child's node becomes the current
+    node and the walk continues with its own distribution; when every child
+    of the current node is rejected (or it has none), the next token is drawn
+    from the residual r there.  T -> 0 is greedy Token Recycling.
+
+    The random numbers are inputs: U [N, K+1] uniforms in [0, 1); the i-th
+    child test at node n compares U[n, i] with r(x) (accept when smaller), and
+    the draw at the final node n* is the inverse CDF of r at U[n*, K] over
+    token IDs in ascending order (the smallest v with r(0) + ... + r(v) >
+    U[n*, K]).  logits [N, V]: the target's logits at every node.
+
+    Returns (acc_len, path, committed, bonus, margin): margin is the smallest
+    distance between a uniform and the threshold it was compared with (for
+    the draw, the distance of U[n*, K] to the CDF at the chosen token and at
+    the one before it), so a caller can tell a decision that fp32 arithmetic
+    could flip."""
+    K1 = np.asarray(U).shape[1]
+    n, path, margin = 0, [0], np.inf
+    while True:
+        r = target_probs(logits[n], T)
+        moved = False
+        for i, c in enumerate(plan.children[n]):
+            x = int(tok[c])
+            u = float(U[n, i])
+            margin = min(margin, abs(u - r[x]))
+            if u < min(1.0, r[x]):
+                n = c
+                path.append(c)
+                moved = True
+                break
+            r[x] = 0.0       # max(0, r - onehot(x)): every other entry is at most 1
+            r = r / r.sum()
+        if not moved:
+            break
+    u = float(U[n, K1 - 1])
+    cdf = np.cumsum(r)
+    y = int(np.searchsorted(cdf, u, side="right"))
+    if y >= len(r):                          # rounding left the total just below u
+        y = int(np.nonzero(r > 0)[0][-1])
+    margin = min(margin, abs(cdf[y] - u), abs(u - (cdf[y - 1] if y > 0 else 0.0)))
+    committed = [int(tok[m]) for m in path[1:]] + [y]
+    return plan.depth[n], path, committed, y, margin
+
+
 def update(M, tok, ids, plan, mode=UPD_ALL, path=None):
     """Overwrite the matrix rows of the verified nodes with their top-K.
 

@@ -53,6 +53,10 @@ class TreePlan:
                 p.append(m)
                 m = parent[m]
             self.path.append(p[::-1])
+        # children[n]: the child nodes of n in rank order
+        self.children = [[] for _ in range(self.N)]
+        for n in range(1, self.N):
+            self.children[parent[n]].append(n)
         # mask[i, j]: tree node j is visible to node i (j is i or an ancestor)
         self.mask = np.zeros((self.N, self.N), dtype=bool)
         for i in range(self.N):

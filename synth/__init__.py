@@ -36,6 +36,7 @@ _C2 = 0x94D049BB133111EB
 TAG_NEXT, TAG_ALT, TAG_NOISE, TAG_PREFIX, TAG_WARM = 1, 2, 3, 4, 5
 TAG_Q, TAG_KT, TAG_VT, TAG_KC, TAG_VC = 6, 7, 8, 9, 10
 TAG_ROOT, TAG_H, TAG_W, TAG_CLASS, TAG_E, TAG_G = 11, 12, 13, 14, 15, 16
+TAG_U = 17
 
 N_ALT = 7            # seeded alternates per token
 BOOST_NEXT = 6.0     # logit boost of the Markov successor
@@ -341,6 +342,19 @@ def initial_cache(w: Workload, cap=None):
         kc[b, :, :L[b]] = kc_rows(w.seed, b, hh, pp, w.d).reshape(w.Hkv, L[b], w.d)
         vc[b, :, :L[b]] = vc_rows(w.seed, b, hh, pp, w.d).reshape(w.Hkv, L[b], w.d)
     return kc, vc
+
+
+# ----------------------------------------------------------------------------
+# uniforms for acceptance under sampling
+# ----------------------------------------------------------------------------
+
+def uniforms(seed, step, b, N, K1):
+    """[N, K1] uniforms in [0, 1) for sequence b at one step: entry (n, j) is
+    the top 24 bits of output j of the stream keyed on (seed, step, b, n),
+    times 2^-24, so every value is exact in fp32 and fp64."""
+    key = hkey(seed, TAG_U, step, b, np.arange(N))
+    j = np.arange(K1)
+    return ((stream(key[:, None], j[None, :]) >> np.uint64(40)).astype(np.float64) * 2.0 ** -24).astype(np.float32)
 
 
 # ----------------------------------------------------------------------------

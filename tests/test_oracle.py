@@ -353,6 +353,42 @@ def test_init_modes():
     assert np.array_equal(R, oracle.init_matrix(oracle.INIT_RANDOM, 500, 8, seed=7))
 
 
+# published reference outputs of splitmix64 (Steele, Lea, Flood 2014, as in
+# Vigna's splitmix64.c): the first outputs of the streams at states 0 and 1234567
+SPLITMIX64_STATE0 = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+SPLITMIX64_STATE1234567 = [6457827717110365317, 3203168211198807973, 9817491932198370423,
+                           4593380528125082431, 16408922859458223821]
+
+
+def test_splitmix64_published_outputs():
+    assert [oracle.mix64_stream(0, i) for i in range(3)] == SPLITMIX64_STATE0
+    assert [oracle.mix64_stream(1234567, i) for i in range(5)] == SPLITMIX64_STATE1234567
+    # the input module's restatement of the same generator agrees
+    assert [int(x) for x in synth.stream(1234567, np.arange(5))] == SPLITMIX64_STATE1234567
+
+
+def test_init_random_index_formula():
+    """RANDOM entry (seq, i, j) is stream output (seq*V + i)*K + j, modulo V.
+
+    Pinned on the published outputs (so a transposed index, a dropped seq
+    term or an off-by-one in the stream index fails), then on a larger
+    matrix against the input module's independent restatement."""
+    o = SPLITMIX64_STATE0
+    R = oracle.init_matrix(oracle.INIT_RANDOM, 7, 2, seed=0)
+    assert R[0, 0] == o[0] % 7 and R[0, 1] == o[1] % 7 and R[1, 0] == o[2] % 7
+    p = SPLITMIX64_STATE1234567
+    R = oracle.init_matrix(oracle.INIT_RANDOM, 5, 1, seed=1234567)
+    assert R[:, 0].tolist() == [x % 5 for x in p]
+    R = oracle.init_matrix(oracle.INIT_RANDOM, 3, 1, seed=1234567, seq=1)
+    assert R[0, 0] == p[3] % 3 and R[1, 0] == p[4] % 3
+    V, K, seed = 37, 5, 99
+    for seq in (0, 2):
+        R = oracle.init_matrix(oracle.INIT_RANDOM, V, K, seed=seed, seq=seq, dtype=np.int32)
+        i, j = np.meshgrid(np.arange(V), np.arange(K), indexing="ij")
+        ref = synth.stream(seed, (seq * V + i) * K + j) % np.uint64(V)
+        assert np.array_equal(R, ref.astype(np.int64))
+
+
 def test_splitmix64_is_a_bijection_on_a_sample():
     # the output function of splitmix64 is invertible: distinct states give distinct outputs
     outs = {oracle.mix64_stream(s, 0) for s in range(20000)}
@@ -446,3 +482,137 @@ def test_t6_expected_tokens_per_pass_chain():
     assert abs(want - 3.3616) < 1e-12
     sd = math.sqrt(2.0 / trials) * 1.5
     assert abs(total / trials - want) < 4 * sd
+
+
+# ----------------------------------------------------------------------------
+# acceptance under sampling (lesson, the acceptance rule; hyper.ai summary,
+# "Experiment": robustness under sampling)
+# ----------------------------------------------------------------------------
+
+def test_softmax_stats_against_logsumexp():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(21)
+    for T in (0.3, 1.0, 2.5):
+        row = rng.normal(size=5000) * 3
+        m, Z = oracle.softmax_stats(row, T)
+        assert m == row.max()
+        assert abs(m / T + math.log(Z) - logsumexp(row / T)) < 1e-9
+        p = oracle.target_probs(row, T)
+        assert abs(p.sum() - 1) < 1e-12 and abs(p[np.argmax(row)] - 1 / Z) < 1e-15
+    assert oracle.softmax_stats(np.full(77, 1.25), 0.7) == (1.25, 77.0)   # equal logits: Z = V
+
+
+def test_sampled_acceptance_hand_case():
+    """Worked by hand from the rule: root distribution [.1, .2, .3, .4] with
+    children holding tokens 3 then 1; U = .5 rejects 3 (.5 >= .4), the residual
+    becomes [1/6, 1/3, 1/2, 0], U = .3 accepts 1 (.3 < 1/3); at that leaf the
+    draw at U = .05 over [.7, .1, .1, .1] gives token 0, at U = .75 token 1."""
+    plan = TreePlan([2, 0, 0], 4)
+    tok = np.array([2, 3, 1])
+    logits = np.log(np.array([[.1, .2, .3, .4], [.25, .25, .25, .25], [.7, .1, .1, .1]]))
+    U = np.zeros((3, 5))
+    U[0, 0], U[0, 1], U[2, 4] = 0.5, 0.3, 0.05
+    acc, path, com, bonus, _ = oracle.accept_sampled(plan, tok, logits, 1.0, U)
+    assert (acc, path, com, bonus) == (1, [0, 2], [1, 0], 0)
+    U[2, 4] = 0.75
+    assert oracle.accept_sampled(plan, tok, logits, 1.0, U)[2] == [1, 1]
+    # both children rejected (.5 >= .4, .4 >= 1/3): draw from [1/6, 1/3, 1/2, 0] at U = .6 -> token 2
+    U[0, 1], U[0, 4] = 0.4, 0.6
+    acc, path, com, bonus, margin = oracle.accept_sampled(plan, tok, logits, 1.0, U)
+    assert (acc, path, com, bonus) == (0, [0], [2], 2)
+    assert abs(margin - min(0.1, 0.4 - 1 / 3, 0.6 - 0.5, 1.0 - 0.6)) < 1e-12
+
+
+def _distinct_sibling_tokens(plan, V, rng):
+    tok = np.zeros(plan.N, np.int64)
+    tok[0] = rng.integers(0, V)
+    for n in range(plan.N):
+        kids = plan.children[n]
+        tok[kids] = rng.choice(V, size=len(kids), replace=False)
+    return tok
+
+
+def test_sampled_acceptance_greedy_limit():
+    """T -> 0 turns sampling into greedy Token Recycling: with distinct sibling
+    tokens (so at most one child can match) the sampled walk equals the
+    greedy acceptance on random tiny trees, whatever the uniforms."""
+    rng = np.random.default_rng(23)
+    for _ in range(300):
+        K = int(rng.integers(1, 5))
+        counts = [int(rng.integers(1, K + 1))]
+        while len(counts) < 1 + sum(counts) and len(counts) < 30:
+            counts.append(int(rng.integers(0, K + 1)) if sum(counts) < 25 else 0)
+        counts += [0] * (1 + sum(counts) - len(counts))
+        plan = TreePlan(counts, K)
+        V = 12
+        tok = _distinct_sibling_tokens(plan, V, rng)
+        logits = rng.permuted(np.tile(np.arange(V, dtype=np.float64), (plan.N, 1)), axis=1)  # distinct values
+        for n in range(1, plan.N):               # make many children match their parent's argmax
+            if rng.random() < 0.6:
+                row = logits[plan.parent[n]]
+                j = int(np.argmax(row))
+                row[[j, tok[n]]] = row[[tok[n], j]]
+        U = rng.random((plan.N, K + 1))
+        got = oracle.accept_sampled(plan, tok, logits, 1e-3, U)[:4]
+        assert got == oracle.accept(plan, tok, np.argmax(logits, axis=1))
+
+
+def test_sampled_first_tokens_follow_the_target():
+    """Losslessness in distribution (lesson): the first committed token is
+    distributed as the root's p = softmax(x / T), and after a first token that
+    a child holds, the second is distributed as that child's p -- whatever the
+    drafted children were.  Chi-square over 30000 draws with uniform U."""
+    from scipy.stats import chisquare
+    rng = np.random.default_rng(29)
+    V, T, n = 6, 0.7, 30000
+    plan = TreePlan([3, 0, 0, 0], 6)
+    tok = np.array([0, 2, 0, 5])
+    logits = rng.normal(size=(4, V)) * 1.5
+    first = np.zeros(V, np.int64)
+    second = np.zeros(V, np.int64)
+    for _ in range(n):
+        com = oracle.accept_sampled(plan, tok, logits, T, rng.random((4, 7)))[2]
+        first[com[0]] += 1
+        if com[0] == 5:
+            second[com[1]] += 1
+    p0 = oracle.target_probs(logits[0], T)
+    assert chisquare(first, p0 * n).pvalue > 1e-3
+    p3 = oracle.target_probs(logits[3], T)
+    assert chisquare(second, p3 * second.sum()).pvalue > 1e-3
+    # the test has power: the same counts against a permuted distribution fail it
+    assert chisquare(first, p0[[1, 2, 3, 4, 0, 5]] * n).pvalue < 1e-6
+
+
+def test_sampled_expected_tokens_per_pass_chain():
+    """Lesson: a linear draft of gamma tokens, each accepted with probability
+    alpha, emits (1 - alpha^(gamma+1)) / (1 - alpha) tokens per pass.  Under
+    the sampling rule a deterministic draft token is accepted with its target
+    probability, so a chain whose every draft token has p = 0.8 must emit
+    3.3616 tokens per pass on average."""
+    gamma, alpha, V, trials = 4, 0.8, 50, 40000
+    plan = TreePlan(synth.chain_tree(gamma), 1)
+    tok = np.arange(plan.N) + 3
+    logits = np.full((plan.N, V), math.log((1 - alpha) / (V - 1)))
+    for n in range(gamma):
+        logits[n, tok[n + 1]] = math.log(alpha)
+    rng = np.random.default_rng(31)
+    total = sum(len(oracle.accept_sampled(plan, tok, logits, 1.0, rng.random((plan.N, 2)))[2])
+                for _ in range(trials))
+    want = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    assert abs(total / trials - want) < 0.03      # about 5 standard errors
+
+
+def test_sampling_loop_at_vanishing_temperature_is_greedy_decoding():
+    """The whole loop under sampling at T = 1e-7 (logits on a 2^-16 grid, so
+    any two distinct values differ by over 150 / T-units) commits exactly the
+    plain greedy stream, like greedy Token Recycling."""
+    V, K, seed = 64, 8, 9
+    plan = TreePlan(synth.TREE_T80, K)
+    target = _synth_target(seed, V)
+    for b in range(2):
+        st = oracle.TRState(M=synth.warm_matrix(seed, b, V, K), root=5 + b, L=100)
+        oracle.tr_loop(plan, [st], target, 10, K, seqs=[b], temperature=1e-7,
+                       uniforms=lambda s, bb: synth.uniforms(seed, s, bb, plan.N, K + 1))
+        ref = oracle.greedy_decode(lambda pos, x: int(np.argmax(target(b, pos, [x])[0])), 5 + b, 100,
+                                   len(st.emitted))
+        assert st.emitted == ref and len(st.emitted) >= 10
