@@ -615,7 +615,7 @@ def main():
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 attention (fp32 accumulate), %s logits, int64/int32 state" % wl.logits,
-        "data": "synthetic (seeded splitmix64 target; see DESIGN.md)",
+        "data": "synthetic: seeded splitmix64 Markov-plus-noise target logits, Irwin-Hall bf16 attention operands",
         "config": config_of(args, wl, world), "timed": "record-then-replay: hot-path kernels only",
         "tree_tokens_per_s": value * wl.B * N,
         "committed_tokens_per_s": world * res["committed"] / (res["total_ms"] * 1e-3),

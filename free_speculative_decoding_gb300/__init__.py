@@ -73,6 +73,7 @@ _SIGS = {
     "tr_step_workspace_bytes": (_sz, [ctypes.POINTER(tr_step_args)]),
     "tr_get_status": (_i, [ctypes.POINTER(ctypes.c_int32), _p]),
     "tr_workspace_clear": (_i, [_p, _sz, _p]),
+    "tr_set_wait_limit_ns": (_i, [_u64, ctypes.POINTER(_u64)]),
     "tr_status_string": (ctypes.c_char_p, [_i]),
     "trsyn_logits": (_i, [_u64, _i, _i64, _p, _p, _p, _i, _p, _i64, _p]),
     "trsyn_rows_bf16": (_i, [_u64, _i, _i64, _i, _i, _i, _i, _p, _p]),
@@ -308,6 +309,17 @@ def tr_step_workspace_bytes(args):
 
 def tr_step(args):
     _check("tr_step", lib().tr_step(ctypes.byref(args), _stream()))
+
+
+def tr_set_wait_limit_ns(ns):
+    """Sets the limit of every bounded device wait for later launches; returns the previous one."""
+    prev = _u64()
+    _check("tr_set_wait_limit_ns", lib().tr_set_wait_limit_ns(int(ns), ctypes.byref(prev)))
+    return prev.value
+
+
+def tr_workspace_clear(ws):
+    _check("tr_workspace_clear", lib().tr_workspace_clear(_ptr(ws), ws.numel() * ws.element_size(), _stream()))
 
 
 def tr_get_status():

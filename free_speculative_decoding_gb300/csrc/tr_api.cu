@@ -2,14 +2,18 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "tr_internal.cuh"
 
 static __device__ unsigned int tr_dev_status_word = 0;
 
 #define TR_MAX_DEVICES 64
-static unsigned int *g_status_ptr[TR_MAX_DEVICES];
-static int g_arch_ok[TR_MAX_DEVICES];  // 0 unknown, 1 ok, -1 unsupported
-static int g_sm_count[TR_MAX_DEVICES];
+// per-device caches, filled on a device's first call; atomic so that first
+// calls from several host threads at once are well defined
+static std::atomic<unsigned int *> g_status_ptr[TR_MAX_DEVICES];
+static std::atomic<int> g_arch_ok[TR_MAX_DEVICES];  // 0 unknown, 1 ok, -1 unsupported
+static std::atomic<int> g_sm_count[TR_MAX_DEVICES];
 
 static int current_device() {
   int dev = -1;
@@ -20,12 +24,14 @@ static int current_device() {
 unsigned int *tr_status_dev() {
   int dev = current_device();
   if (dev < 0) return nullptr;
-  if (!g_status_ptr[dev]) {
+  unsigned int *s = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (!s) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, tr_dev_status_word) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = (unsigned int *)p;
+    s = (unsigned int *)p;
+    g_status_ptr[dev].store(s, std::memory_order_release);
   }
-  return g_status_ptr[dev];
+  return s;
 }
 
 int tr_check_device() {
@@ -34,16 +40,16 @@ int tr_check_device() {
     cudaGetLastError();
     return TR_E_CUDA;
   }
-  if (g_arch_ok[dev] == 0) {
+  if (g_arch_ok[dev].load() == 0) {
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return TR_E_CUDA;
-    g_sm_count[dev] = sms;
-    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    g_sm_count[dev].store(sms);
+    g_arch_ok[dev].store((major == 10 && minor == 3) ? 1 : -1);
   }
-  if (g_arch_ok[dev] < 0) return TR_E_UNSUPPORTED;
+  if (g_arch_ok[dev].load() < 0) return TR_E_UNSUPPORTED;
   if (!tr_status_dev()) return TR_E_CUDA;
   return TR_OK;
 }
@@ -51,8 +57,9 @@ int tr_check_device() {
 int tr_sm_count() {
   int dev = current_device();
   if (dev < 0) return 148;
-  if (g_sm_count[dev] == 0) tr_check_device();
-  return g_sm_count[dev] > 0 ? g_sm_count[dev] : 148;
+  if (g_sm_count[dev].load() == 0) tr_check_device();
+  const int n = g_sm_count[dev].load();
+  return n > 0 ? n : 148;
 }
 
 // ---------------------------------------------------------------------------
@@ -144,6 +151,17 @@ extern "C" int tr_get_status(int32_t *host_out, tr_stream_t stream) {
   TR_TRY_CUDA(cudaMemcpy(tr_status_dev(), &zero, sizeof(zero), cudaMemcpyHostToDevice));
   *host_out = (int32_t)v;
   return v ? TR_E_DEVICE : TR_OK;
+}
+
+static std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+
+unsigned long long tr_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+extern "C" int tr_set_wait_limit_ns(uint64_t ns, uint64_t *previous) {
+  if (ns < 1 || ns > 60000000000ull) return TR_E_INVAL;
+  const unsigned long long old = g_wait_limit_ns.exchange(ns);
+  if (previous) *previous = old;
+  return TR_OK;
 }
 
 extern "C" int tr_workspace_clear(void *ws, size_t ws_bytes, tr_stream_t stream) {

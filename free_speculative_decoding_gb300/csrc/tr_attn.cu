@@ -114,6 +114,7 @@ struct AttnArgs {
   int B, N, Hq, Hkv, G, HG, cap;
   int q_rows, c_rows, t_rows;  // TMA box heights (at most the tensor's extent)
   float scale_log2;
+  unsigned long long wait_ns;  // limit of every bounded wait
 };
 
 __device__ __forceinline__ int tiles_per_pair(int Lb, int N) { return (Lb + BN - 1) / BN + (N + BN - 1) / BN; }
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   // every wait of the warp-wide roles is warp-uniform: a lane that gives up
   // takes its whole warp with it, so warp-collective instructions stay converged
   auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
-    const bool mine = mbar_wait(bar, parity, abort);
+    const bool mine = mbar_wait(bar, parity, abort, a.wait_ns);
     const bool all = __all_sync(0xffffffffu, mine);
     if (!all) give_up();
     return all;
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           const bool cache = j < sg.n_ct;
           const int s = cnt % NS;
           const uint32_t ph = (cnt / NS) & 1;
-          if (!mbar_wait(&empty[s], ph ^ 1, abort)) {
+          if (!mbar_wait(&empty[s], ph ^ 1, abort, a.wait_ns)) {
             give_up();
             ok = false;
             break;
@@ -723,7 +724,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         mbar_arrive(&bars->mrg_in);
         if (threadIdx.x == 128) {
           int is_last = 0;
-          if (mbar_wait(&bars->mrg_in, n_split & 1, abort)) {
+          if (mbar_wait(&bars->mrg_in, n_split & 1, abort, a.wait_ns)) {
             __threadfence();
             is_last = atomicAdd(&a.cnt[sg.pair], 1) == c1 - c0;
             __threadfence();
@@ -891,6 +892,7 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
   a.c_rows = (int)c_rows;
   a.t_rows = (int)t_rows;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_ns = tr_wait_limit_ns();
   cudaStream_t s = (cudaStream_t)stream;
   const int grid = launch_grid(p, B, Hkv, cap, N);
   static bool attr_set[1][64];

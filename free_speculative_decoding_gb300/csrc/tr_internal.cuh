@@ -65,6 +65,7 @@ __device__ __forceinline__ float tr_key_val(unsigned long long k) { return tr_un
 // ---------------------------------------------------------------------------
 
 int tr_check_device();  // TR_OK on an sm_103 device, else TR_E_UNSUPPORTED / TR_E_CUDA
+unsigned long long tr_wait_limit_ns();  // limit of the bounded device waits (tr_set_wait_limit_ns)
 int tr_sm_count();
 
 #define TR_TRY_CUDA(expr)                         \
@@ -85,5 +86,8 @@ static inline int tr_kmax(int K) { return K <= 8 ? 8 : (K <= 16 ? 16 : 32); }
 
 // top-K internals shared with the step and the LM head
 size_t tr_topk_counters_offset(int64_t rows, int64_t V, int K);  // byte offset of the arrival counters in the workspace
+// stats != NULL: also each row's (max, sum of exp((x - max) / temperature)) into stats [rows, 2]
+// (16-byte aligned rows only: the caller checks)
 int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K,
-                   int32_t *ids, float *vals, void *ws, size_t ws_bytes, cudaStream_t stream);
+                   int32_t *ids, float *vals, void *ws, size_t ws_bytes, cudaStream_t stream,
+                   float temperature = 1.f, float *stats = nullptr);

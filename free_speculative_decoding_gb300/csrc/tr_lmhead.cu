@@ -46,7 +46,8 @@ struct Bars {
 template <int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int rows,
-                     long long V, int D, int n_mt, int n_nt, unsigned long long *part, unsigned *status) {
+                     long long V, int D, int n_mt, int n_nt, unsigned long long *part, unsigned *status,
+                     unsigned long long wait_ns) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
-          if (!mbar_wait(&bars->empty[s], ph ^ 1, abort)) {
+          if (!mbar_wait(&bars->empty[s], ph ^ 1, abort, wait_ns)) {
             give_up();
             break;
           }
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the loop, so control flow and operands stay
     // warp-uniform; one elected lane issues the MMAs and commits.
     auto wwait = [&](uint64_t *bar, uint32_t parity) -> bool {
-      const bool all = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
+      const bool all = __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, wait_ns));
       if (!all && lane == 0) give_up();
       return all;
     };
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int mt = t % n_mt, nt = t / n_mt;
       const int acc = tc & 1;
       const uint32_t aph = (tc >> 1) & 1;
-      if (!mbar_wait(&bars->tfull[acc], aph, abort)) {
+      if (!mbar_wait(&bars->tfull[acc], aph, abort, wait_ns)) {
         give_up();
         break;
       }
@@ -291,7 +292,7 @@ int launch(const CUtensorMap &ta, const CUtensorMap &tb, long long rows, int D, 
   const int tiles = n_mt * n_nt;
   const int grid = tiles < tr_sm_count() ? tiles : tr_sm_count();
   lmhead_tc_kernel<KMAX><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, (int)rows, V, D, n_mt, n_nt, part,
-                                                            tr_status_dev());
+                                                            tr_status_dev(), tr_wait_limit_ns());
   merge_lists_kernel<KMAX><<<(unsigned)((rows + 3) / 4), 128, 0, s>>>(part, rows, n_nt, K, ids, vals);
   return TR_OK;
 }

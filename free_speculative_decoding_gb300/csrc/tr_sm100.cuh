@@ -77,15 +77,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// try_wait may suspend the thread in hardware for a while before it reports
+// an incomplete phase, which would hide limits shorter than that suspension;
+// limits below this are enforced by polling with the non-blocking test_wait.
+constexpr uint64_t kPollBelowNs = 100000ull;
+
 // Waits for the phase with the given parity to complete.  Gives up and
 // returns false when *abort becomes non-zero (another role gave up) or after
 // limit_ns nanoseconds, so no wait can spin forever.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort,
                                           uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool poll = limit_ns < kPollBelowNs;
+  if (poll ? mbar_test(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll ? mbar_test(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
@@ -93,9 +99,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
 
 // Waits for the phase with the given parity; false after limit_ns nanoseconds.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool poll = limit_ns < kPollBelowNs;
+  if (poll ? mbar_test(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
+  while (!(poll ? mbar_test(bar, parity) : mbar_try_wait(bar, parity)))
     if (globaltimer_ns() - t0 > limit_ns) return false;
   return true;
 }

@@ -10,6 +10,12 @@ namespace {
 
 constexpr int kThreads = 256;  // >= TR_MAX_NODES: one thread per tree node
 
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // retrieval: one warp expands the tree level by level
 // ---------------------------------------------------------------------------
@@ -294,8 +300,16 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(const uint4 *Kt, const
 // (BFS order), which both resolves duplicate writes and lets the retrieval
 // take a rewritten row from the new top-K rows it already holds, so it never
 // waits for its own global writes.  CTAs 1..G copy the accepted K/V rows
-// (each evaluates the cheap acceptance itself); the last of them to finish
-// advances L (CTA 0 does when there is no KV cache).
+// (each evaluates the cheap acceptance itself from tree_tok); the last of them
+// to finish advances L (CTA 0 does when there is no KV cache).
+//
+// tree_tok is both this step's tree (read by every CTA of the sequence) and
+// the next step's tree (the output), so it is overwritten only once every CTA
+// of the sequence has read it: each commit CTA counts itself in `loaded[b]`
+// after loading, and CTA 0 counts itself after leaving the next tree in
+// `stash[b]`.  Whoever arrives last writes tree_tok (CTA 0 straight from
+// shared memory, a commit CTA by copying the stash) and resets the counter.
+// No CTA waits for another, so any grid size and any scheduling order works.
 struct FinishArgs {
   void *M;
   long long V;
@@ -307,7 +321,9 @@ struct FinishArgs {
   uint4 *Kc, *Vc;
   int cap, Hkv, d16, heads_per_cta;
   int mode;
-  unsigned *counters;
+  unsigned *counters;  // [B] commit CTAs finished (the last advances L)
+  unsigned *loaded;    // [B] CTAs that have read this step's tree_tok
+  int32_t *stash;      // [B, N] the next tree, when a commit CTA arrives last
   unsigned *status;
 };
 
@@ -352,6 +368,19 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(FinishArgs a, const __
     }
   }
   load_tree_state(tree, a.tree_tok + (long long)b * N, ids_b, K, s, part == 0 ? ids_s : nullptr);
+  if (part > 0) {
+    // this CTA has read tree_tok; the last of the sequence's CTAs writes the next tree
+    if (n == 0) {
+      __threadfence();
+      s.last = atomicAdd(&a.loaded[b], 1u) == (unsigned)G;
+    }
+    __syncthreads();
+    if (s.last) {
+      __threadfence();
+      if (n < N) a.tree_tok[(long long)b * N + n] = __ldcg(a.stash + (long long)b * N + n);
+      if (n == 0) a.loaded[b] = 0u;
+    }
+  }
   block_accept(tree, s);
   const int acc = s.acc_len;
   if (part == 0) {
@@ -401,8 +430,30 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(FinishArgs a, const __
         }
         __syncwarp();
       }
-      int32_t *out = a.tree_tok + (long long)b * N;
-      for (int m = lane; m < N; m += 32) out[m] = next_tok[m];
+      // publish the next tree once every commit CTA has read this step's
+      bool direct = G == 0;
+      if (!direct) {
+        unsigned seen = 0;
+        if (lane == 0) seen = ld_acquire_u32(&a.loaded[b]);
+        seen = __shfl_sync(0xffffffffu, seen, 0);
+        if (seen == (unsigned)G) {
+          direct = true;  // all of them already have: no arrival is left to come
+        } else {
+          int32_t *st = a.stash + (long long)b * N;
+          for (int m = lane; m < N; m += 32) st[m] = next_tok[m];
+          __threadfence();
+          __syncwarp();
+          unsigned prev = 0;
+          if (lane == 0) prev = atomicAdd(&a.loaded[b], 1u);
+          prev = __shfl_sync(0xffffffffu, prev, 0);
+          direct = prev == (unsigned)G;  // the others arrived meanwhile
+        }
+        if (direct && lane == 0) a.loaded[b] = 0u;
+      }
+      if (direct) {
+        int32_t *out = a.tree_tok + (long long)b * N;
+        for (int m = lane; m < N; m += 32) out[m] = next_tok[m];
+      }
       if (lane == 0) {
         a.root[b] = s.bonus;
         if (G == 0) {
@@ -514,16 +565,20 @@ extern "C" int tr_kv_commit(const void *Kt, const void *Vt, void *Kc, void *Vc, 
   return TR_OK;
 }
 
-// workspace of tr_step: [top-K workspace | commit counters]
+// workspace of tr_step: [top-K workspace | commit counters [B] | tree-read
+// counters [B] | next-tree stash [B, N]], each part 256-byte aligned
 static size_t step_topk_ws(const tr_step_args *a) {
   const int64_t rows = (int64_t)a->B * a->tree->dev.N;
   if (a->logits) return tr_align_up(tr_topk_workspace_bytes(rows, a->V, a->K), 256);
   return tr_align_up(tr_lmhead_topk_workspace_bytes(rows, a->D, a->V, a->K), 256);
 }
 
+static size_t step_counters_bytes(int B) { return tr_align_up((size_t)B * 4, 256); }
+
 extern "C" size_t tr_step_workspace_bytes(const tr_step_args *a) {
   if (!a || !a->tree || a->B < 1) return 0;
-  return step_topk_ws(a) + tr_kv_commit_workspace_bytes(a->B);
+  return step_topk_ws(a) + 2 * step_counters_bytes(a->B) +
+         tr_align_up((size_t)a->B * a->tree->dev.N * 4, 256);
 }
 
 extern "C" int tr_step(const tr_step_args *a, tr_stream_t stream) {
@@ -570,6 +625,8 @@ extern "C" int tr_step(const tr_step_args *a, tr_stream_t stream) {
   f.heads_per_cta = commit ? commit_heads_per_cta(a->Hkv) : 1;
   f.mode = a->mode;
   f.counters = (unsigned *)((char *)a->ws + tk_ws);
+  f.loaded = (unsigned *)((char *)a->ws + tk_ws + step_counters_bytes(a->B));
+  f.stash = (int32_t *)((char *)a->ws + tk_ws + 2 * step_counters_bytes(a->B));
   f.status = tr_status_dev();
   const int G = commit ? (a->Hkv + f.heads_per_cta - 1) / f.heads_per_cta : 0;  // commit CTAs per sequence
   if (a->mtype == TR_I64)

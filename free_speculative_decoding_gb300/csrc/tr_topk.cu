@@ -148,10 +148,28 @@ __device__ __forceinline__ void write_final(int32_t *ids, float *vals, long long
   }
 }
 
-template <typename T, int KMAX>
+// (max, Z) of a row from the lanes' running pairs: Z = sum of 2^((x - max) c).
+__device__ __forceinline__ float2 warp_stats(float m, float z, float c) {
+  float M = m;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+  float S = m == -INFINITY ? 0.f : z * sm100::ex2((m - M) * c);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) S += __shfl_xor_sync(kFull, S, off);
+  return make_float2(M, S);
+}
+
+// STATS: also the row's softmax statistics at temperature T, c = log2(e) / T:
+// stats[row] = (max, sum of exp((x - max) / T)), from a running (max, sum) per
+// lane over the elements it examines (exp2 with the sum rescaled when the
+// lane's maximum grows), combined over the lanes at the end of a row segment
+// and, for a row split between warps, over the segments by the merging warp
+// (pstats holds one pair per list slot).
+template <typename T, int KMAX, bool STATS>
 __global__ void __launch_bounds__(kWarps * 32, 1)
     topk_warp_kernel(const T *__restrict__ x, long long V, long long ld, int K, int nch, long long U, int32_t *ids,
-                     float *vals, unsigned long long *part, unsigned *counters, unsigned *status) {
+                     float *vals, unsigned long long *part, unsigned *counters, unsigned *status,
+                     unsigned long long wait_ns, float c, float2 *stats, float2 *pstats) {
   using namespace sm100;
   extern __shared__ unsigned char smem_raw[];
   const int lane = threadIdx.x & 31;
@@ -173,14 +191,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   float thr = 0.f;
   long long cur = -1;   // row of the segment
   int seg_first = 0, seg_units = 0;
+  float st_m = -INFINITY, st_z = 0.f;  // STATS: this lane's running maximum and sum
 
   // end of a row segment: the final list, or this segment's list for a merge
   auto flush = [&](long long row) {
+    float2 rs = make_float2(0.f, 0.f);
+    if (STATS) rs = warp_stats(st_m, st_z, c);
     if (seg_first == 0 && seg_units == nch) {
       write_final(ids, vals, row, K, lane, lk);
+      if (STATS && lane == 0) stats[row] = rs;
       return;
     }
     if (lane < K) part[((unsigned long long)row * nch + seg_first) * KMAX + lane] = lk;
+    if (STATS && lane == 0) pstats[(unsigned long long)row * nch + seg_first] = rs;
     __threadfence();
     __syncwarp();
     unsigned last = 0;
@@ -192,15 +215,27 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     L.init();
     const long long r0 = row * nch;
     const long long wlo = warp_of(r0, U, W), whi = warp_of(r0 + nch - 1, U, W);
+    float pm = -INFINITY, pz = 0.f;  // STATS: the segments' pairs this lane folds
     for (long long p = wlo + lane; p <= whi; p += 32) {
       const long long sp = range_start(p, U, W);
       if (sp >= range_start(p + 1, U, W)) continue;  // a warp without steps
       const long long first = (sp > r0 ? sp : r0) - r0;
       const unsigned long long *src = part + ((unsigned long long)row * nch + first) * KMAX;
       for (int j = 0; j < K; ++j) list_insert(L.k, __ldcg(src + j));
+      if (STATS) {
+        const float2 q = __ldcg(pstats + (unsigned long long)row * nch + first);
+        const float nm = fmaxf(pm, q.x);
+        pz = (pm == -INFINITY ? 0.f : pz * sm100::ex2((pm - nm) * c)) +
+             (q.x == -INFINITY ? 0.f : q.y * sm100::ex2((q.x - nm) * c));
+        pm = nm;
+      }
     }
     const unsigned long long m = warp_merge<KMAX>(L, lane);
     write_final(ids, vals, row, K, lane, m);
+    if (STATS) {
+      const float2 q = warp_stats(pm, pz, c);
+      if (lane == 0) stats[row] = q;
+    }
     if (lane == 0) counters[row] = 0u;  // the workspace is left zeroed
   };
 
@@ -241,17 +276,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
   };
 
-  auto process = [&](int q, long long r, int c) {
+  auto process = [&](int q, long long r, int cc) {
     if (r != cur) {
       if (cur >= 0) flush(cur);
       cur = r;
       lk = 0ull;
       have_k = false;
-      seg_first = c;
+      seg_first = cc;
       seg_units = 0;
+      st_m = -INFINITY;
+      st_z = 0.f;
     }
     ++seg_units;
-    const long long off = (long long)c * kStep;
+    const long long off = (long long)cc * kStep;
     const long long nb = min(row_bytes - off, (long long)kStep);
     const long long id0 = off / (long long)sizeof(T);                      // first element of the step
     const long long et = id0 + (nb >> 4) * kV;                              // first element past the vectors
@@ -279,6 +316,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       return m;
     };
     float lm = lane_max();
+    if (STATS && !isnan(lm)) {
+      // every element of the step enters the lane's running sum, before the
+      // top-K passes below clear any of them from the stage
+      const float nm = fmaxf(st_m, lm), nmc = nm * c;
+      float z4[4] = {st_m == -INFINITY ? 0.f : st_z * sm100::ex2((st_m - nm) * c), 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < kVecs; ++j) {
+        if (j * 32 + lane < nvec) {
+          float e[kV];
+          Elem<T>::unpack(sv[j * 32 + lane], e);
+#pragma unroll
+          for (int qq = 0; qq < kV; ++qq) z4[qq & 3] += sm100::ex2(fmaf(e[qq], c, -nmc));
+        }
+      }
+      if (!isnan(tv)) z4[1] += sm100::ex2(fmaf(tv, c, -nmc));
+      st_z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+      st_m = nm;
+    }
     // An element enters only above the floor f: the K-th best value held,
     // when there is one (the held keys all come from earlier steps, with
     // lower IDs, so only a strictly larger value can enter); else the K-th
@@ -344,16 +399,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   };
 
   long long r = u0 / nch;
-  int c = (int)(u0 - r * nch);
+  int cs = (int)(u0 - r * nch);
   int q = 0;
   uint32_t ph = 0;
   int i = 0;
   for (; i < n_steps; ++i) {
-    if (!__all_sync(kFull, mbar_wait_for(&ring.full[q], ph))) break;
-    process(q, r, c);
+    if (!__all_sync(kFull, mbar_wait_for(&ring.full[q], ph, wait_ns))) break;
+    process(q, r, cs);
     refill(q);
-    if (++c == nch) {
-      c = 0;
+    if (++cs == nch) {
+      cs = 0;
       ++r;
     }
     if (++q == kStages) {
@@ -475,9 +530,10 @@ size_t part_bytes_for(long long rows, long long V, int K) {
   return tr_align_up((size_t)rows * (size_t)steps_per_row(V, 4) * tr_kmax(K) * 8, 256);
 }
 
-template <typename T, int KMAX>
+template <typename T, int KMAX, bool STATS>
 cudaError_t launch_warp(const void *logits, long long rows, long long V, long long ld, int K, int32_t *ids,
-                        float *vals, unsigned long long *part, unsigned *counters, cudaStream_t s) {
+                        float *vals, unsigned long long *part, unsigned *counters, float c, float2 *stats,
+                        float2 *pstats, cudaStream_t s) {
   const int nch = (int)steps_per_row(V, sizeof(T));
   const long long U = rows * nch;
   const long long want = (U + kWarps - 1) / kWarps;
@@ -487,13 +543,14 @@ cudaError_t launch_warp(const void *logits, long long rows, long long V, long lo
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(topk_warp_kernel<T, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
+    const cudaError_t e = cudaFuncSetAttribute(topk_warp_kernel<T, KMAX, STATS>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  topk_warp_kernel<T, KMAX><<<grid, kWarps * 32, kRingSmem, s>>>((const T *)logits, V, ld, K, nch, U, ids, vals, part,
-                                                                 counters, tr_status_dev());
+  topk_warp_kernel<T, KMAX, STATS><<<grid, kWarps * 32, kRingSmem, s>>>(
+      (const T *)logits, V, ld, K, nch, U, ids, vals, part, counters, tr_status_dev(), tr_wait_limit_ns(), c, stats,
+      pstats);
   return cudaGetLastError();
 }
 
@@ -523,13 +580,20 @@ cudaError_t launch_scan(const void *logits, long long rows, long long V, long lo
                             part, counters);
 }
 
+// Workspace layout: [list slots | row counters | STATS: one (max, sum) pair per list slot].
+size_t counters_bytes_for(long long rows) { return tr_align_up((size_t)rows * 4, 256); }
+size_t pstats_bytes_for(long long rows, long long V) { return tr_align_up((size_t)rows * steps_per_row(V, 4) * 8, 256); }
+
 template <typename T, int KMAX>
 cudaError_t launch(const void *logits, long long rows, long long V, long long ld, int K, int32_t *ids, float *vals,
-                   void *ws, cudaStream_t s) {
+                   void *ws, float c, float2 *stats, cudaStream_t s) {
   unsigned long long *part = (unsigned long long *)ws;
   unsigned *counters = (unsigned *)((char *)ws + (ws ? part_bytes_for(rows, V, K) : 0));
+  float2 *pstats = (float2 *)((char *)ws + (ws ? part_bytes_for(rows, V, K) + counters_bytes_for(rows) : 0));
   const bool aligned = ((uintptr_t)logits % 16 == 0) && ((ld * (long long)sizeof(T)) % 16 == 0);
-  if (aligned) return launch_warp<T, KMAX>(logits, rows, V, ld, K, ids, vals, part, counters, s);
+  if (stats) return launch_warp<T, KMAX, true>(logits, rows, V, ld, K, ids, vals, part, counters, c, stats, pstats, s);
+  if (aligned)
+    return launch_warp<T, KMAX, false>(logits, rows, V, ld, K, ids, vals, part, counters, 0.f, nullptr, nullptr, s);
   return launch_scan<T, KMAX>(logits, rows, V, ld, K, ids, vals, part, counters, s);
 }
 
@@ -538,16 +602,17 @@ cudaError_t launch(const void *logits, long long rows, long long V, long long ld
 extern "C" size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K) {
   if (rows <= 0 || V <= 0 || K < 1 || K > TR_MAX_K) return 0;
   if (steps_per_row(V, 4) == 1) return 0;  // no row is ever split
-  return part_bytes_for(rows, V, K) + tr_align_up((size_t)rows * 4, 256);
+  return part_bytes_for(rows, V, K) + counters_bytes_for(rows) + pstats_bytes_for(rows, V);
 }
 
 size_t tr_topk_counters_offset(int64_t rows, int64_t V, int K) { return part_bytes_for(rows, V, K); }
 
 int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K, int32_t *ids,
-                   float *vals, void *ws, size_t ws_bytes, cudaStream_t s) {
+                   float *vals, void *ws, size_t ws_bytes, cudaStream_t s, float temperature, float *stats) {
   (void)ws_bytes;
   const int km = tr_kmax(K);
-#define TR_TOPK_CASE(T, KM) launch<T, KM>(logits, rows, V, ld, K, ids, vals, ws, s)
+  const float c = stats ? 1.4426950408889634f / temperature : 0.f;
+#define TR_TOPK_CASE(T, KM) launch<T, KM>(logits, rows, V, ld, K, ids, vals, ws, c, (float2 *)stats, s)
   cudaError_t e;
   if (ftype == TR_F32)
     e = km == 8 ? TR_TOPK_CASE(float, 8) : km == 16 ? TR_TOPK_CASE(float, 16) : TR_TOPK_CASE(float, 32);
@@ -573,4 +638,23 @@ extern "C" int tr_topk(const void *logits, tr_ftype ftype, int64_t rows, int64_t
   int rc = tr_check_device();
   if (rc != TR_OK) return rc;
   return tr_topk_launch(logits, ftype, rows, V, ld, K, ids, vals, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int tr_topk_softmax(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K,
+                               float temperature, int32_t *ids, float *vals, float *stats, void *ws, size_t ws_bytes,
+                               tr_stream_t stream) {
+  if (rows < 0 || V < 1 || K < 1 || K > TR_MAX_K || K > V || ld < V) return TR_E_INVAL;
+  if (ftype != TR_F32 && ftype != TR_BF16) return TR_E_INVAL;
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return TR_E_INVAL;
+  if (V > INT32_MAX) return TR_E_UNSUPPORTED;
+  if (rows == 0) return TR_OK;
+  if (!logits || !ids || !stats) return TR_E_INVAL;
+  const size_t esz = ftype == TR_F32 ? 4 : 2;
+  if ((uintptr_t)logits % 16 || (ld * (int64_t)esz) % 16) return TR_E_UNSUPPORTED;  // streamed rows only
+  const size_t need = tr_topk_workspace_bytes(rows, V, K);
+  if (need && (!ws || ws_bytes < need)) return TR_E_INVAL;
+  int rc = tr_check_device();
+  if (rc != TR_OK) return rc;
+  return tr_topk_launch(logits, ftype, rows, V, ld, K, ids, vals, ws, ws_bytes, (cudaStream_t)stream, temperature,
+                        stats);
 }

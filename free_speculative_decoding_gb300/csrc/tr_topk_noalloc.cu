@@ -15,23 +15,27 @@
 // stand-in, never a device address, so its device address is looked up with
 // cudaGetSymbolAddress once per device (on that device's first call, with the
 // device current) and passed to the kernel.
+#include <atomic>
+
 #include "tr_internal.cuh"
 
 static __device__ __align__(256) unsigned char g_topk_scratch[TR_TOPK_NOALLOC_SCRATCH_BYTES];
 
 #define TR_NOALLOC_MAX_DEVICES 64
-static void *g_scratch_addr[TR_NOALLOC_MAX_DEVICES];
+// per-device address cache; atomic so that first calls from several host
+// threads at once are well defined (they all store the same address)
+static std::atomic<void *> g_scratch_addr[TR_NOALLOC_MAX_DEVICES];
 
 // Device address of this device's scratch array (looked up once per device).
 static int scratch_address(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= TR_NOALLOC_MAX_DEVICES) return TR_E_CUDA;
-  if (!g_scratch_addr[dev]) {
-    void *p = nullptr;
+  void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || !p) return TR_E_CUDA;
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return TR_OK;
 }
 

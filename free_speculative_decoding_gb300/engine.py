@@ -55,12 +55,17 @@ class TRState:
         self.ws_step = workspace(tr_step_workspace_bytes(self._args), device)
 
     def start(self, root, L, M_src=None, mode=TR_INIT_INHERIT, seed=0):
-        """Set the roots and cache lengths, initialise M, retrieve the first tree."""
+        """Set the roots and cache lengths, initialise M, retrieve the first tree.
+
+        M_src [B, V, K] is copied in as it is; M_src [V, K] is inherited by
+        every sequence (tr_init_matrix INHERIT); without M_src, ``mode`` is
+        TR_INIT_ZERO or TR_INIT_RANDOM (at ``seed``), or None to keep M as it
+        already is."""
         self.root.copy_(torch.as_tensor(root, dtype=torch.int32))
         self.L.copy_(torch.as_tensor(L, dtype=torch.int32))
         if M_src is not None and M_src.dim() == 3:
             self.M.copy_(M_src)
-        else:
+        elif mode is not None:
             tr_init_matrix(self.M, mode, M_src, seed)
         tr_retrieve(self.M, self.tree, self.root, self.tree_tok)
 

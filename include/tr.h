@@ -316,6 +316,20 @@ size_t tr_step_workspace_bytes(const tr_step_args *args);
  * and clears it.  Returns TR_OK when the word was 0, TR_E_DEVICE otherwise. */
 int tr_get_status(int32_t *host_out, tr_stream_t stream);
 
+/* Time limit of every bounded device wait (the tensor-core kernels' mbarrier
+ * waits for copies and products, the top-K's waits for its bulk copies), in
+ * nanoseconds, for the launches made after this call in this process; the
+ * default is 2 s.  A wait that runs out sets TR_DEV_TIMEOUT, the kernel lets
+ * the copies and products it has issued complete and returns, so the context
+ * stays usable; the results of that launch are undefined and its workspace
+ * must be cleared (tr_workspace_clear) before the next call that uses it.  A
+ * limit far below a kernel's normal waits makes every launch give up: that is
+ * how the timeout path is tested (limits under 100 us are enforced by polling,
+ * since a hardware-suspended wait could outlast them).  ns in [1, 6e10];
+ * *previous (may be NULL)
+ * receives the limit that was in force.  TR_E_INVAL outside the range. */
+int tr_set_wait_limit_ns(uint64_t ns, uint64_t *previous);
+
 /* Zeroes a workspace (cudaMemsetAsync on stream). */
 int tr_workspace_clear(void *ws, size_t ws_bytes, tr_stream_t stream);
 

@@ -48,15 +48,31 @@ def oracle_qkv(w, seqs=None):
     return qkv
 
 
-def oracle_states(w, seqs=None, with_cache=True):
+INIT_SEED = 0x5EED_0F_7E57   # seed of tr_init_matrix(RANDOM) in the loop tests
+
+
+def oracle_matrix(w, b, init="warm"):
+    """Sequence b's starting matrix on the oracle side.
+
+    "warm": the synthetic inherited matrix of sequence b (the GPU copies it in,
+    or inherits it through tr_init_matrix); "zero" / "random": what
+    tr_init_matrix leaves (random at INIT_SEED)."""
+    dt = np.int64 if w.m_dtype == "int64" else np.int32
+    if init == "zero":
+        return oracle.init_matrix(oracle.INIT_ZERO, w.V, w.K, dtype=dt)
+    if init == "random":
+        return oracle.init_matrix(oracle.INIT_RANDOM, w.V, w.K, seed=INIT_SEED, seq=b, dtype=dt)
+    return synth.warm_matrix(w.seed, b, w.V, w.K).astype(dt)
+
+
+def oracle_states(w, seqs=None, with_cache=True, init="warm"):
     seqs = range(w.B) if seqs is None else seqs
     L0 = w.prefix_lengths()
     roots = synth.initial_roots(w)
-    dt = np.int64 if w.m_dtype == "int64" else np.int32
     states = []
     cap = w.capacity()
     for b in seqs:
-        st = oracle.TRState(M=synth.warm_matrix(w.seed, b, w.V, w.K).astype(dt), root=int(roots[b]), L=int(L0[b]))
+        st = oracle.TRState(M=oracle_matrix(w, b, init), root=int(roots[b]), L=int(L0[b]))
         if with_cache and w.attention:
             st.kc = np.zeros((w.Hkv, cap, w.d), np.float32)
             st.vc = np.zeros((w.Hkv, cap, w.d), np.float32)
@@ -67,11 +83,36 @@ def oracle_states(w, seqs=None, with_cache=True):
     return states
 
 
-def run_gpu_loop(w, steps, record=True, keep_M_every=1, o_seqs=None, o_steps=None, device="cuda"):
+def gpu_start(w, st, init="warm"):
+    """Initialise the matrices of a TRState and retrieve the first trees.
+
+    "warm": every sequence inherits its own synthetic matrix through
+    tr_init_matrix(INHERIT) (one call per sequence); "zero" / "random":
+    tr_init_matrix over the whole batch."""
+    import free_speculative_decoding_gb300 as tr
+    from synth import device as sd
+    roots, L0 = synth.initial_roots(w), w.prefix_lengths()
+    if init == "warm":
+        sd.warm_matrices(w, st)
+        src = st.M.clone()
+        for b in range(w.B):
+            tr.tr_init_matrix(st.M[b:b + 1], tr.TR_INIT_INHERIT, src[b])
+        st.start(roots, L0, M_src=None, mode=None)
+    elif init == "zero":
+        st.start(roots, L0, M_src=None, mode=tr.TR_INIT_ZERO)
+    elif init == "random":
+        st.start(roots, L0, M_src=None, mode=tr.TR_INIT_RANDOM, seed=INIT_SEED)
+    else:
+        raise ValueError(init)
+
+
+def run_gpu_loop(w, steps, record=True, keep_M_every=1, o_seqs=None, o_steps=None, device="cuda",
+                 init="warm", mode=0):
     """Run `steps` Token Recycling steps of workload w on the GPU; return per-step records.
 
     Attention outputs are kept for the sequences ``o_seqs`` at the steps
-    ``o_steps`` (all by default)."""
+    ``o_steps`` (all by default).  ``init`` picks the starting matrices
+    (gpu_start), ``mode`` the update rule (TR_UPD_ALL or TR_UPD_ACCEPTED)."""
     import free_speculative_decoding_gb300 as tr
     from free_speculative_decoding_gb300.engine import TRState
     from synth import device as sd
@@ -83,10 +124,9 @@ def run_gpu_loop(w, steps, record=True, keep_M_every=1, o_seqs=None, o_steps=Non
     st = TRState(tree, w.B, w.V, m_dtype=mdt, Hq=w.Hq if w.attention else 0, Hkv=w.Hkv, d=w.d, cap=cap,
                  logits_dtype=ldt, D=w.D if w.logits == "lmhead" else 0, device=device)
     tgt = sd.DeviceTarget(w, tree, device)
-    sd.warm_matrices(w, st)
     if w.attention:
         sd.fill_cache(w, st)
-    st.start(synth.initial_roots(w), w.prefix_lengths(), M_src=st.M.clone())
+    gpu_start(w, st, init)
     recs = []
     for s in range(steps):
         rec = {"tok": st.tree_tok.cpu().numpy().copy(), "L": st.L.cpu().numpy().copy()}
@@ -99,9 +139,9 @@ def run_gpu_loop(w, steps, record=True, keep_M_every=1, o_seqs=None, o_steps=Non
                 rec["O"] = O.cpu().numpy().copy()
                 rec["O_seqs"] = list(range(w.B)) if o_seqs is None else list(o_seqs)
         if w.logits == "lmhead":
-            st.finish(H=tgt.hidden_for(st), Wt=tgt.Wt, Kt=kt, Vt=vt)
+            st.finish(H=tgt.hidden_for(st), Wt=tgt.Wt, Kt=kt, Vt=vt, mode=mode)
         else:
-            st.finish(logits=tgt.logits_for(st), Kt=kt, Vt=vt)
+            st.finish(logits=tgt.logits_for(st), Kt=kt, Vt=vt, mode=mode)
         if record:
             rec.update(ids=st.ids.cpu().numpy().reshape(w.B, tree.N, w.K).copy(),
                        vals=st.vals.cpu().numpy().reshape(w.B, tree.N, w.K).copy(),

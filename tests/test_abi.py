@@ -134,3 +134,13 @@ def test_step_and_noalloc_validation_before_any_launch(lib):
     assert lib.tr_topk_noalloc(p, tr.TR_F32, 70000, 10, 10, 3, p, None, None) == tr.TR_E_UNSUPPORTED  # rows
     assert lib.tr_topk_noalloc(p, tr.TR_BF16, 60000, 128256, 128256, 8, p, None,
                                None) == tr.TR_E_UNSUPPORTED                                           # scratch
+
+
+def test_wait_limit_is_host_state(lib):
+    """tr_set_wait_limit_ns only records the limit later launches take (no GPU needed)."""
+    import free_speculative_decoding_gb300 as tr
+    prev = ctypes.c_uint64()
+    assert lib.tr_set_wait_limit_ns(0, ctypes.byref(prev)) == tr.TR_E_INVAL
+    assert lib.tr_set_wait_limit_ns(61_000_000_000, None) == tr.TR_E_INVAL
+    assert tr.tr_set_wait_limit_ns(5000) == 2_000_000_000
+    assert tr.tr_set_wait_limit_ns(2_000_000_000) == 5000

@@ -30,12 +30,12 @@ def built():
     b.build()
 
 
-def _check_loop(w, steps, seqs=None, attn=True, M_every=1):
+def _check_loop(w, steps, seqs=None, attn=True, M_every=1, init="warm", mode=0):
     plan = oracle.TreePlan(w.child_counts, w.K)
-    recs, st, status = run_gpu_loop(w, steps, keep_M_every=M_every)
+    recs, st, status = run_gpu_loop(w, steps, keep_M_every=M_every, init=init, mode=mode)
     assert status == 0
     seqs = list(range(w.B)) if seqs is None else list(seqs)
-    states = oracle_states(w, seqs, with_cache=attn and w.attention)
+    states = oracle_states(w, seqs, with_cache=attn and w.attention, init=init)
     target = target_fn(w)
 
     def on_step(s, i, rec):
@@ -44,7 +44,7 @@ def _check_loop(w, steps, seqs=None, attn=True, M_every=1):
         if "M" in recs[s]:
             assert np.array_equal(recs[s]["M"][b], states[i].M), "M after step %d seq %d" % (s, b)
 
-    oracle.tr_loop(plan, states, target, steps, w.K,
+    oracle.tr_loop(plan, states, target, steps, w.K, mode=mode,
                    qkv=oracle_qkv(w, seqs) if (attn and w.attention) else None,
                    scale=w.d ** -0.5, on_step=on_step, seqs=seqs)
     return recs
@@ -87,6 +87,51 @@ def test_lmhead_loop_reduced():
     """Fused LM head (D=4096, V=32000) feeding accept and update."""
     w = synth.WORKLOADS["lmhead"].scaled(B=3, steps=4)
     _check_loop(w, w.steps, attn=False)
+
+
+@pytest.mark.parametrize("init", ["zero", "random", "warm"])
+@pytest.mark.parametrize("mode", [0, 1], ids=["update_all", "update_accepted"])
+def test_init_and_update_ablation_loops(init, mode):
+    """The hyper.ai summary's ablations ("Experiment": all-zero, random and
+    inherited initial matrices; updates from all draft tokens or from the
+    accepted ones only) through the whole GPU loop: tr_init_matrix starts the
+    matrices, tr_step runs with the chosen update rule, and every step's
+    integer state and matrix equal the oracle's."""
+    w = synth.WORKLOADS["batched"].scaled(B=2, steps=5, prefix=(100, 300))
+    _check_loop(w, w.steps, init=init, mode=mode)
+
+
+def test_loop_from_random_init_full_vocab():
+    """The tiny workload's loop started from tr_init_matrix(RANDOM) at V=32000
+    instead of a copied matrix."""
+    w = synth.WORKLOADS["tiny"].scaled(steps=6)
+    _check_loop(w, w.steps, init="random")
+
+
+def test_finish_grid_beyond_one_wave():
+    """128 sequences x (1 + 8) step-end CTAs: more than one wave of the step-end
+    kernel, so some KV-commit CTAs start after their sequence's CTA 0 has left
+    the next tree.  Tree tokens, acceptance, L and every committed cache row
+    must still equal the oracle's."""
+    w = synth.WORKLOADS["batched"].scaled(B=128, V=4096, Hq=8, Hkv=8, prefix=(64, 192), steps=3)
+    plan = oracle.TreePlan(w.child_counts, w.K)
+    recs, st, status = run_gpu_loop(w, w.steps, keep_M_every=1, o_seqs=[0, 77])
+    assert status == 0
+    states = oracle_states(w, range(w.B), with_cache=True)
+    target = target_fn(w)
+
+    def on_step(s, i, rec):
+        compare_step(w, plan, s, i, i, rec, recs[s], attn=i in (0, 77))
+        assert np.array_equal(recs[s]["M"][i], states[i].M), "M after step %d seq %d" % (s, i)
+
+    oracle.tr_loop(plan, states, target, w.steps, w.K, qkv=oracle_qkv(w), scale=w.d ** -0.5, on_step=on_step)
+    Lg = st.L.cpu().numpy()
+    Kc = st.Kc.float().cpu().numpy()
+    Vc = st.Vc.float().cpu().numpy()
+    for b in range(w.B):
+        assert Lg[b] == states[b].L
+        assert np.array_equal(Kc[b, :, :Lg[b]], states[b].kc[:, :Lg[b]]), "K cache of seq %d" % b
+        assert np.array_equal(Vc[b, :, :Lg[b]], states[b].vc[:, :Lg[b]]), "V cache of seq %d" % b
 
 
 def test_accepted_only_update_mode():
