@@ -57,10 +57,16 @@ def load_peaks():
     return PEAK_FALLBACK, "fallback"
 
 
+U_SEED = 0xACC_E97   # seed of the acceptance uniforms under sampling
+INIT_SEED = 0x5EED_0F_7E57
+
+
 def config_of(args, wl, world):
     """The workload as both arms name it in their JSON line."""
     return {"workload": args.workload, "B": wl.B, "V": wl.V, "K": wl.K, "tree": wl.tree, "tree_nodes": wl.N,
             "tree_depth": wl.depth(), "prefix": list(wl.prefix), "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+            "acceptance": ("greedy" if args.temperature is None else "sampled at T=%g" % args.temperature),
+            "init": args.init, "update": args.update,
             "parallelism": "replicas (dp%d, no collective)" % world,
             "l2": ("every step reads its own recorded hidden rows; the weight (V x D bf16) is larger than L2"
                    if wl.logits == "lmhead" else
@@ -203,11 +209,12 @@ def run_gpu(args, rank, world):
     st = TRState(tree, w.B, w.V, m_dtype=mdt, Hq=w.Hq if w.attention else 0, Hkv=w.Hkv, d=w.d, cap=cap,
                  logits_dtype=ldt, D=w.D if lm else 0, device=dev)
     tgt = sd.DeviceTarget(w, tree, dev)
-    sd.warm_matrices(w, st)
     if w.attention:
         sd.fill_cache(w, st)
-    st.start(synth.initial_roots(w), w.prefix_lengths(), M_src=st.M.clone())
+    start_matrices(args, w, st)
     stream = torch.cuda.current_stream()
+    T = args.temperature
+    upd = tr.TR_UPD_ACCEPTED if args.update == "accepted" else tr.TR_UPD_ALL
 
     # per-step input sizes
     if lm:
@@ -215,6 +222,8 @@ def run_gpu(args, rank, world):
     else:
         step_in = w.B * N * w.V * (2 if w.logits == "bf16" else 4)
     qkv_b = w.B * N * w.d * 2 * (w.Hq + 2 * w.Hkv) if w.attention else 0
+    if T is not None:
+        step_in += w.B * N * (w.K + 1) * 4   # the acceptance uniforms
     budget = args.store_gb * 2 ** 30
     seg = max(1, min(K, int(budget // max(1, step_in + qkv_b))))
 
@@ -228,6 +237,8 @@ def run_gpu(args, rank, world):
             bufs["q"] = torch.empty(n, w.B, N, w.Hq, w.d, dtype=torch.bfloat16, device=dev)
             bufs["kt"] = torch.empty(n, w.B, N, w.Hkv, w.d, dtype=torch.bfloat16, device=dev)
             bufs["vt"] = torch.empty(n, w.B, N, w.Hkv, w.d, dtype=torch.bfloat16, device=dev)
+        if T is not None:
+            bufs["U"] = torch.empty(n, w.B, N, w.K + 1, dtype=torch.float32, device=dev)
         return bufs
 
     bufs = make_bufs(seg)
@@ -242,6 +253,8 @@ def run_gpu(args, rank, world):
             tgt.hidden_for(st, bufs["H"][i])
         else:
             tgt.logits_for(st, bufs["logits"][i])
+        if T is not None:
+            tr.trsyn_uniforms(U_SEED, s, bufs["U"][i])
         gstep[0] += 1
 
     def hot_step(i, ev=None):
@@ -254,9 +267,11 @@ def run_gpu(args, rank, world):
         if ev is not None:
             ev[1].record(stream)
         if lm:
-            st.finish(H=bufs["H"][i], Wt=tgt.Wt, Kt=kt, Vt=vt)
+            st.finish(H=bufs["H"][i], Wt=tgt.Wt, Kt=kt, Vt=vt, mode=upd)
+        elif T is not None:
+            st.finish(logits=bufs["logits"][i], Kt=kt, Vt=vt, mode=upd, temperature=T, U=bufs["U"][i])
         else:
-            st.finish(logits=bufs["logits"][i], Kt=kt, Vt=vt)
+            st.finish(logits=bufs["logits"][i], Kt=kt, Vt=vt, mode=upd)
         if ev is not None:
             ev[2].record(stream)
 
@@ -368,6 +383,24 @@ def run_gpu(args, rank, world):
     return res
 
 
+def start_matrices(args, w, st):
+    """Initial matrices and first trees: the workload's synthetic inherited
+    matrices (each sequence inherits its own through tr_init_matrix), or an
+    all-zero / random start (tr_init_matrix over the batch)."""
+    import free_speculative_decoding_gb300 as tr
+    from synth import device as sd
+    roots, L0 = synth.initial_roots(w), w.prefix_lengths()
+    if args.init == "inherit":
+        sd.warm_matrices(w, st)
+        src = st.M.clone()
+        for b in range(w.B):
+            tr.tr_init_matrix(st.M[b:b + 1], tr.TR_INIT_INHERIT, src[b])
+        st.start(roots, L0, M_src=None, mode=None)
+    else:
+        st.start(roots, L0, M_src=None, mode=tr.TR_INIT_ZERO if args.init == "zero" else tr.TR_INIT_RANDOM,
+                 seed=INIT_SEED)
+
+
 def run_e2e(args, w, st, tgt, bufs, gen_step, hot_step, snapshot, restore, dev, N, lm):
     """Same steps with every step's inputs copied from pinned host memory and the
     committed tokens read back, all inside the timed region.  The copy of step
@@ -431,11 +464,12 @@ def run_e2e(args, w, st, tgt, bufs, gen_step, hot_step, snapshot, restore, dev, 
 # oracle arm (CPU)
 # ----------------------------------------------------------------------------
 
-def oracle_sequence_step(w, b, state, plan, step):
+def oracle_sequence_step(w, b, state, plan, step, temperature=None, mode=0):
     """One Token Recycling step of sequence b on the CPU oracle; returns seconds
     spent in the method (the synthetic target's logits are made before timing)."""
     import oracle
     depth = np.asarray(plan.depth)
+    U = synth.uniforms(U_SEED, step, b, plan.N, w.K + 1) if temperature is not None else None
     tok = oracle.retrieve(state.M, state.root, plan)
     if w.logits == "lmhead":
         H = synth.bf16_to_f32(synth.lm_hidden_rows(w.seed, b, state.L + depth, tok, w.D))
@@ -454,8 +488,11 @@ def oracle_sequence_step(w, b, state, plan, step):
         if qkv is not None:
             oracle.tree_attention(qkv[0], state.kc, state.vc, state.L, qkv[1], qkv[2], plan, w.d ** -0.5)
     ids, _ = oracle.topk_rows(rows, w.K)
-    acc, path, committed, bonus = oracle.accept(plan, tok, ids[:, 0])
-    oracle.update(state.M, tok, ids, plan)
+    if temperature is None:
+        acc, path, committed, bonus = oracle.accept(plan, tok, ids[:, 0])
+    else:
+        acc, path, committed, bonus, _, _ = oracle.accept_sampled(plan, tok, rows, temperature, U)
+    oracle.update(state.M, tok, ids, plan, mode, path)
     if w.attention and state.kc is not None:
         state.L = oracle.kv_commit(state.kc, state.vc, qkv[1], qkv[2], state.L, path)
     else:
@@ -473,14 +510,24 @@ def _lm_weight_cache(w):
     return _LMW[w.name]
 
 
-def oracle_rate(w, budget_s, max_seq_steps=None):
+def oracle_matrix(w, b, init):
+    import oracle
+    if init == "zero":
+        return oracle.init_matrix(oracle.INIT_ZERO, w.V, w.K)
+    if init == "random":
+        return oracle.init_matrix(oracle.INIT_RANDOM, w.V, w.K, seed=INIT_SEED, seq=b)
+    return synth.warm_matrix(w.seed, b, w.V, w.K)
+
+
+def oracle_rate(w, budget_s, max_seq_steps=None, temperature=None, init="inherit", update="all"):
     """Oracle steps/s of the full batch, extrapolated from a bounded sample of
     sequence-steps of one sequence (each sequence is independent and alike)."""
     import oracle
     plan = oracle.TreePlan(w.child_counts, w.K)
     b = 0
     L0 = int(w.prefix_lengths()[b])
-    st = oracle.TRState(M=synth.warm_matrix(w.seed, b, w.V, w.K), root=int(synth.initial_roots(w)[b]), L=L0)
+    mode = oracle.UPD_ACCEPTED if update == "accepted" else oracle.UPD_ALL
+    st = oracle.TRState(M=oracle_matrix(w, b, init), root=int(synth.initial_roots(w)[b]), L=L0)
     if w.attention:
         cap = L0 + 64 * (plan.max_depth + 1)
         st.kc = np.zeros((w.Hkv, cap, w.d), np.float32)
@@ -490,7 +537,7 @@ def oracle_rate(w, budget_s, max_seq_steps=None):
         st.vc[:, :L0] = synth.bf16_to_f32(synth.vc_rows(w.seed, b, hh, pp, w.d)).reshape(w.Hkv, L0, w.d)
     spent, n = 0.0, 0
     while spent < budget_s and (max_seq_steps is None or n < max_seq_steps) and n < 64:
-        spent += oracle_sequence_step(w, b, st, plan, n)
+        spent += oracle_sequence_step(w, b, st, plan, n, temperature, mode)
         n += 1
     per_seq_step = spent / n
     return 1.0 / (per_seq_step * w.B), n, spent
@@ -514,8 +561,9 @@ def oracle_rate_one_core(args, budget_s, max_seq_steps=None):
             "sys.path.insert(0, %r)\n"
             "import bench\n"
             "w = bench.workload_of(types.SimpleNamespace(workload=%r, tree=%r))\n"
-            "print(json.dumps(bench.oracle_rate(w, %r, %r)))\n"
-            % (ROOT, args.workload, args.tree, float(budget_s), max_seq_steps))
+            "print(json.dumps(bench.oracle_rate(w, %r, %r, %r, %r, %r)))\n"
+            % (ROOT, args.workload, args.tree, float(budget_s), max_seq_steps, args.temperature, args.init,
+               args.update))
     try:
         r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
         rate, n, spent = json.loads(r.stdout.strip().splitlines()[-1])
@@ -541,7 +589,15 @@ def main():
     ap.add_argument("--store-gb", type=float, default=40.0, help="HBM for recorded step inputs")
     ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--temperature", type=float, default=None,
+                    help="acceptance under sampling at this temperature (tr_step_sampled); greedy without it")
+    ap.add_argument("--init", default="inherit", choices=["inherit", "zero", "random"],
+                    help="starting matrices: each sequence's inherited synthetic matrix, all zero, or random")
+    ap.add_argument("--update", default="all", choices=["all", "accepted"],
+                    help="matrix update from every verified node, or from the accepted path only")
     args = ap.parse_args()
+    if args.temperature is not None and synth.WORKLOADS[args.workload].logits == "lmhead":
+        ap.error("sampling needs stored logits: not with the fused LM-head workload")
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -554,8 +610,9 @@ def main():
             return
         per_step = max(1.0, 150.0 / max(1, args.steps + args.warmup))
         import oracle  # noqa: F401
-        oracle_rate(w, budget_s=1e9, max_seq_steps=max(1, args.warmup))   # warm-up steps
-        rate, n, spent = oracle_rate(w, budget_s=per_step * args.steps, max_seq_steps=args.steps)
+        okw = dict(temperature=args.temperature, init=args.init, update=args.update)
+        oracle_rate(w, budget_s=1e9, max_seq_steps=max(1, args.warmup), **okw)   # warm-up steps
+        rate, n, spent = oracle_rate(w, budget_s=per_step * args.steps, max_seq_steps=args.steps, **okw)
         line = {"impl": "reference", "metric": metric, "value": rate, "unit": unit, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / rate, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention / exact compare", "data": "synthetic",
@@ -643,7 +700,8 @@ def main():
         line["e2e"] = {"value": world * e["steps"] / (e["ms"] * 1e-3), "unit": unit, "h2d_bytes_per_step": e["h2d"],
                        "d2h_bytes_per_step": e["d2h"], "steps": e["steps"]}
     # the oracle on a bounded sample of the same workload, on this host's cores
-    rate, n, spent = oracle_rate(wl, budget_s=args.cpu_budget)
+    rate, n, spent = oracle_rate(wl, budget_s=args.cpu_budget, temperature=args.temperature, init=args.init,
+                                 update=args.update)
     line["cpu_baseline"] = {"value": rate, "unit": unit, "cores": cpu_cores(), "kind": "oracle",
                             "sample": "%d sequence-steps of sequence 0 (%.1f s of oracle time), scaled to %d "
                                       "sequences; BLAS calls may use all cores" % (n, spent, wl.B)}

@@ -63,6 +63,9 @@ _SIGS = {
     "tr_topk": (_i, [_p, _i, _i64, _i64, _i64, _i, _p, _p, _p, _sz, _p]),
     "tr_topk_workspace_bytes": (_sz, [_i64, _i64, _i]),
     "tr_topk_noalloc": (_i, [_p, _i, _i64, _i64, _i64, _i, _p, _p, _p]),
+    "tr_topk_softmax": (_i, [_p, _i, _i64, _i64, _i64, _i, _f, _p, _p, _p, _p, _sz, _p]),
+    "tr_accept_sampled": (_i, [_p, _i, _p, _p, _i, _p, _i, _i64, _i64, _p, _f, _p, _p, _p, _p, _p, _p]),
+    "tr_step_sampled": (_i, [ctypes.POINTER(tr_step_args), _f, _p, _p]),
     "tr_lmhead_topk": (_i, [_p, _p, _i64, _i, _i64, _i, _p, _p, _p, _sz, _p]),
     "tr_lmhead_topk_workspace_bytes": (_sz, [_i64, _i, _i64, _i]),
     "tr_accept": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _p, _p]),
@@ -81,6 +84,7 @@ _SIGS = {
     "trsyn_lm_hidden": (_i, [_u64, _i, _i, _p, _p, _p, _p, _p]),
     "trsyn_lm_weight": (_i, [_u64, _i64, _i, _p, _p]),
     "trsyn_warm_matrix": (_i, [_u64, _i, _i64, _i, _i, _p, _p]),
+    "trsyn_uniforms": (_i, [_u64, _i64, _i, _i, _i, _p, _p]),
 }
 
 ABI_SYMBOLS = tuple(_SIGS)
@@ -244,6 +248,30 @@ def tr_topk_noalloc(logits, K, ids, vals, V=None):
                                                     _ptr(vals), _stream()))
 
 
+def tr_topk_softmax(logits, K, temperature, ids, vals, stats, ws, V=None):
+    """tr_topk plus stats [rows, 2] = (row max, sum of exp((x - max) / T))."""
+    rows, ld = logits.shape
+    V = ld if V is None else V
+    _i32(ids, "ids")
+    if stats.dtype != torch.float32:
+        raise ValueError("stats must be float32")
+    _check("tr_topk_softmax", lib().tr_topk_softmax(_ptr(logits), _ftype(logits), rows, V, ld, K, float(temperature),
+                                                    _ptr(ids), _ptr(vals), _ptr(stats),
+                                                    _ptr(ws) if ws is not None else None,
+                                                    ws.numel() if ws is not None else 0, _stream()))
+
+
+def tr_accept_sampled(tree, tree_tok, ids, logits, stats, temperature, U, acc_len, path, committed, bonus, V=None):
+    B = tree_tok.shape[0]
+    K = ids.shape[-1]
+    V = logits.shape[1] if V is None else V
+    if U.dtype != torch.float32 or stats.dtype != torch.float32:
+        raise ValueError("U and stats must be float32")
+    _check("tr_accept_sampled", lib().tr_accept_sampled(
+        tree.handle, B, _ptr(tree_tok), _ptr(ids), K, _ptr(logits), _ftype(logits), V, logits.shape[1], _ptr(stats),
+        float(temperature), _ptr(U), _ptr(acc_len), _ptr(path), _ptr(committed), _ptr(bonus), _stream()))
+
+
 def tr_lmhead_topk_workspace_bytes(rows, D, V, K):
     return lib().tr_lmhead_topk_workspace_bytes(rows, D, V, K)
 
@@ -311,6 +339,12 @@ def tr_step(args):
     _check("tr_step", lib().tr_step(ctypes.byref(args), _stream()))
 
 
+def tr_step_sampled(args, temperature, U):
+    if U.dtype != torch.float32:
+        raise ValueError("U must be float32")
+    _check("tr_step_sampled", lib().tr_step_sampled(ctypes.byref(args), float(temperature), _ptr(U), _stream()))
+
+
 def tr_set_wait_limit_ns(ns):
     """Sets the limit of every bounded device wait for later launches; returns the previous one."""
     prev = _u64()
@@ -363,6 +397,11 @@ def trsyn_lm_hidden(seed, tree, tree_tok, L, out):
 def trsyn_lm_weight(seed, out):
     V, D = out.shape
     _check("trsyn_lm_weight", lib().trsyn_lm_weight(seed, V, D, _ptr(out), _stream()))
+
+
+def trsyn_uniforms(seed, step, out):
+    B, N, K1 = out.shape
+    _check("trsyn_uniforms", lib().trsyn_uniforms(seed, step, B, N, K1, _ptr(out), _stream()))
 
 
 def trsyn_warm_matrix(seed, M):

@@ -84,6 +84,8 @@ extern "C" int tr_tree_create(const int32_t *child_counts, int n_nodes, int K, s
       return TR_E_INVAL;
     }
     t->child_counts[n] = c;
+    d.child_first[n] = (uint8_t)(c ? named : 0);
+    d.child_count[n] = (uint8_t)c;
     for (int r = 0; r < c; ++r) {
       d.parent[named] = (uint8_t)n;
       d.rank[named] = (uint8_t)r;

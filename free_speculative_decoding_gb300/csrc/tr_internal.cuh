@@ -21,6 +21,8 @@ struct TreeDev {
   uint8_t parent[TR_MAX_NODES];         // parent of node n (root: 0)
   uint8_t rank[TR_MAX_NODES];           // child index of n under its parent
   uint8_t depth[TR_MAX_NODES];
+  uint8_t child_first[TR_MAX_NODES];    // children of n are nodes child_first[n] .. + child_count[n] - 1
+  uint8_t child_count[TR_MAX_NODES];    // (BFS order keeps a node's children together, in rank order)
   unsigned long long anc[TR_MAX_NODES][2];  // bit j set iff node j is on the root->n path (n included)
 };
 

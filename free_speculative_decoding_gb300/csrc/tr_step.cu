@@ -69,6 +69,8 @@ struct AcceptSmem {
   int tok[TR_MAX_NODES];
   int top1[TR_MAX_NODES];
   int path[TR_MAX_NODES];
+  float cw[TR_MAX_NODES];  // sampling: node n's weight 2^((x - max) c) in its parent's row
+  float cz[TR_MAX_NODES];  // sampling: node n's normaliser Z (the same units)
   unsigned long long nomatch[2];
   int warp_best[kThreads / 32];
   int best;      // chosen node n*
@@ -161,6 +163,245 @@ __device__ void write_accept_outputs(const TreeDev &tree, const AcceptSmem &s, i
 }
 
 // ---------------------------------------------------------------------------
+// acceptance under sampling
+// ---------------------------------------------------------------------------
+
+// Logits of one row, fp32 or bf16 (widened exactly).
+template <typename LT>
+struct Logit;
+template <>
+struct Logit<float> {
+  static constexpr int kVec = 4;
+  __device__ __forceinline__ static float at(const float *p) { return __ldg(p); }
+  __device__ __forceinline__ static void vec(const float *p, float (&e)[4]) {
+    const float4 q = __ldg(reinterpret_cast<const float4 *>(p));
+    e[0] = q.x;
+    e[1] = q.y;
+    e[2] = q.z;
+    e[3] = q.w;
+  }
+};
+template <>
+struct Logit<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static float at(const __nv_bfloat16 *p) {
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p)) << 16);
+  }
+  __device__ __forceinline__ static void vec(const __nv_bfloat16 *p, float (&e)[8]) {
+    const uint4 q = __ldg(reinterpret_cast<const uint4 *>(p));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      e[2 * i] = __uint_as_float(w[i] << 16);
+      e[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct SampleArgs {
+  const void *logits;  // [B*N, ld] of the logit type
+  long long ld;
+  const float2 *stats; // [B*N] (row maximum, sum of 2^((x - max) c))
+  const float *U;      // [B, N, K1] uniforms in [0, 1)
+  int K1;              // K + 1
+  float c;             // log2(e) / temperature
+};
+
+// Speculative-decoding lesson, the acceptance rule, applied to Token
+// Recycling's deterministic children in rank order (q one-hot on the child's
+// token): child x of the current node is accepted when U < r(x), r being the
+// node's distribution with the already rejected siblings' tokens removed and
+// renormalised; the walk continues from an accepted child and stops at a node
+// whose children are all rejected.  In units of the row maximum, r(x) is
+// w(x) / (Z - sum of the rejected distinct tokens' w).  Every CTA of the
+// sequence computes the same walk (thread 0; the weights come in one parallel
+// gather).  Sets s.best, s.acc_len and s.path.
+template <typename LT>
+__device__ void block_accept_sampled(const TreeDev &tree, AcceptSmem &s, const SampleArgs &sa, int b, long long V,
+                                     unsigned *status) {
+  const int n = threadIdx.x, N = tree.N;
+  if (n < N) {
+    const long long rown = (long long)b * N + n;
+    s.cz[n] = sa.stats[rown].y;
+    if (n > 0) {
+      const long long rowp = (long long)b * N + tree.parent[n];
+      const int x = s.tok[n];
+      float w = 0.f;
+      if (x >= 0 && (long long)x < V) {
+        const float l = Logit<LT>::at((const LT *)sa.logits + rowp * sa.ld + x);
+        w = ex2_approx(fmaf(l, sa.c, -sa.stats[rowp].x * sa.c));
+      } else {
+        tr_flag(status, TR_DEV_BAD_TOKEN);
+      }
+      s.cw[n] = w;
+    }
+  }
+  __syncthreads();
+  if (n == 0) {
+    int cur = 0;
+    while (true) {
+      const int f = tree.child_first[cur], cnt = tree.child_count[cur];
+      const float *u = sa.U + ((long long)b * N + cur) * sa.K1;
+      float rem = s.cz[cur];
+      int next = -1;
+      for (int i = 0; i < cnt; ++i) {
+        const int ch = f + i, x = s.tok[ch];
+        bool dup = false;  // an earlier (rejected) sibling holds the same token: r(x) is 0 now
+        for (int j = 0; j < i; ++j) dup |= s.tok[f + j] == x;
+        const float w = s.cw[ch];
+        const float r = dup ? 0.f : w / fmaxf(rem, w);
+        if (__ldg(u + i) < r) {
+          next = ch;
+          break;
+        }
+        if (!dup) rem -= w;
+      }
+      if (next < 0) break;
+      cur = next;
+    }
+    s.best = cur;
+    s.acc_len = tree.depth[cur];
+  }
+  __syncthreads();
+  if (n < N && ((tree.anc[s.best][n >> 6] >> (n & 63)) & 1ull)) s.path[tree.depth[n]] = n;
+  __syncthreads();
+}
+
+// The draw at the final node n*: the smallest token y with
+// r(0) + ... + r(y) > U[n*, K], r being n*'s distribution without its
+// (rejected) children's tokens.  Each thread sums the weights of a contiguous
+// chunk of the row (compensated fp32 sums), a block scan of the chunk sums in
+// fp64 finds the chunk where the running sum crosses U times the total, and
+// that chunk's thread walks it.  The weights' own fp32 rounding (~1e-6
+// relative) is then the only error of the running sum.  Loads go in batches of
+// whole 16-byte vectors (every chunk starts on one).  Returns y on every thread.
+template <typename LT>
+__device__ int block_draw_residual(const TreeDev &tree, AcceptSmem &s, const SampleArgs &sa, int b, long long V) {
+  constexpr int VW = Logit<LT>::kVec, BV = 8;  // elements per vector, vectors per batch
+  __shared__ double wsum[kThreads / 32 + 1];
+  __shared__ int winner, last_pos;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, N = tree.N;
+  const int nstar = s.best;
+  const long long row = (long long)b * N + nstar;
+  const LT *x = (const LT *)sa.logits + row * sa.ld;
+  const float mc = sa.stats[row].x * sa.c;
+  const float u = __ldg(sa.U + row * sa.K1 + (sa.K1 - 1));
+  const int f = tree.child_first[nstar], cnt = tree.child_count[nstar];
+  long long C = (V + kThreads - 1) / kThreads;
+  C = (C + VW - 1) / VW * VW;
+  const long long lo = min(V, (long long)t * C), hi = min(V, lo + C);
+  bool any_rej = false;  // does a rejected child's token fall in this chunk?
+  for (int i = 0; i < cnt; ++i) {
+    const int xr = s.tok[f + i];
+    any_rej |= xr >= lo && xr < hi;
+  }
+  auto weight = [&](long long v, float l) -> float {
+    if (any_rej)
+      for (int i = 0; i < cnt; ++i)
+        if (s.tok[f + i] == v) return 0.f;
+    return ex2_approx(fmaf(l, sa.c, -mc));  // -inf (past the chunk) gives 0
+  };
+  auto load_batch = [&](long long v0, float (&e)[BV][VW]) {
+#pragma unroll
+    for (int j = 0; j < BV; ++j) {
+      const long long vj = v0 + j * VW;
+      if (vj + VW <= hi) {
+        Logit<LT>::vec(x + vj, e[j]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < VW; ++q) e[j][q] = vj + q < hi ? Logit<LT>::at(x + vj + q) : -INFINITY;
+      }
+    }
+  };
+  // compensated (Kahan) running sum in fp32: sum - comp tracks the exact sum closely
+  struct Kahan {
+    float sum = 0.f, comp = 0.f;
+    __device__ __forceinline__ void add(float e) {
+      const float y = e - comp;
+      const float tt = sum + y;
+      comp = (tt - sum) - y;
+      sum = tt;
+    }
+    __device__ __forceinline__ double value() const { return (double)sum - (double)comp; }
+  };
+  // pass 1: the chunk's sum, element by element in token order
+  Kahan k1;
+  for (long long v0 = lo; v0 < hi; v0 += BV * VW) {
+    float e[BV][VW];
+    load_batch(v0, e);
+#pragma unroll
+    for (int j = 0; j < BV; ++j)
+#pragma unroll
+      for (int q = 0; q < VW; ++q) k1.add(weight(v0 + j * VW + q, e[j][q]));
+  }
+  const double z = k1.value();
+  // exclusive and inclusive prefix of the chunk sums (fp64): incl of thread t
+  // is bitwise the excl of thread t + 1, so the chunks' intervals tile [0, total)
+  double incl = z;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  const double excl_w = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (t == 0) {
+    winner = -1;
+    last_pos = -1;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (t == 0) {
+    double acc = 0.0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const double tw = wsum[w];
+      wsum[w] = acc;
+      acc += tw;
+    }
+    wsum[kThreads / 32] = acc;
+  }
+  __syncthreads();
+  const double woff = wsum[warp];
+  const double total = wsum[kThreads / 32];
+  incl += woff;
+  const double excl = lane == 0 ? woff : excl_w + woff;
+  const double target = (double)u * total;
+  if (excl <= target && target < incl) winner = t;
+  if (z > 0.0) atomicMax(&last_pos, t);
+  __syncthreads();
+  // no chunk claims u * total only through rounding (u * total == total): the last chunk with weight
+  const int wt = winner >= 0 ? winner : last_pos;
+  if (t == 0 && wt < 0) s.bonus = s.top1[nstar];  // no weight left at all (the children held it all)
+  if (t == wt) {
+    // pass 2: the same compensated sum, element by element, until it passes the target
+    Kahan k2;
+    long long y = -1, last_tok = -1;
+    for (long long v0 = lo; v0 < hi && y < 0; v0 += BV * VW) {
+      float e[BV][VW];
+      load_batch(v0, e);
+#pragma unroll
+      for (int j = 0; j < BV; ++j)
+#pragma unroll
+        for (int q = 0; q < VW; ++q) {
+          const long long v = v0 + j * VW + q;
+          const float w = weight(v, e[j][q]);
+          if (w > 0.f) last_tok = v;
+          k2.add(w);
+          if (y < 0 && w > 0.f && excl + k2.value() > target) y = v;
+        }
+    }
+    s.bonus = (int)(y >= 0 ? y : last_tok);
+  }
+  __syncthreads();
+  return s.bonus;
+}
+
+// ---------------------------------------------------------------------------
 // update: M[tok[n]] <- ids[n] for the writing nodes, last in BFS order wins
 // ---------------------------------------------------------------------------
 
@@ -225,6 +466,20 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const __grid_constant_
   const int b = blockIdx.x;
   load_tree_state(tree, tree_tok + (long long)b * tree.N, ids + (long long)b * tree.N * K, K, s);
   block_accept(tree, s);
+  write_accept_outputs(tree, s, b, acc_len, path, committed, bonus);
+}
+
+template <typename LT>
+__global__ void __launch_bounds__(kThreads) accept_sampled_kernel(const __grid_constant__ TreeDev tree,
+                                                                  const int32_t *tree_tok, const int32_t *ids, int K,
+                                                                  long long V, SampleArgs sa, int32_t *acc_len,
+                                                                  int32_t *path, int32_t *committed, int32_t *bonus,
+                                                                  unsigned *status) {
+  __shared__ AcceptSmem s;
+  const int b = blockIdx.x;
+  load_tree_state(tree, tree_tok + (long long)b * tree.N, ids + (long long)b * tree.N * K, K, s);
+  block_accept_sampled<LT>(tree, s, sa, b, V, status);
+  block_draw_residual<LT>(tree, s, sa, b, V);
   write_accept_outputs(tree, s, b, acc_len, path, committed, bonus);
 }
 
@@ -325,6 +580,7 @@ struct FinishArgs {
   unsigned *loaded;    // [B] CTAs that have read this step's tree_tok
   int32_t *stash;      // [B, N] the next tree, when a commit CTA arrives last
   unsigned *status;
+  SampleArgs sa;       // acceptance under sampling (SAMPLE kernels only)
 };
 
 constexpr int kHash = 2 * TR_MAX_NODES;  // open addressing, load factor <= 1/2
@@ -352,7 +608,11 @@ struct WriterTable {
   }
 };
 
-template <typename T>
+// SAMPLE: the acceptance samples at a temperature (block_accept_sampled and,
+// in CTA 0, block_draw_residual for the committed token after the path); LT
+// is then the logits' element type.  The matrix update, the KV commit and the
+// next retrieval are the same either way.
+template <typename T, typename LT, bool SAMPLE>
 __global__ void __launch_bounds__(kThreads) finish_kernel(FinishArgs a, const __grid_constant__ TreeDev tree) {
   __shared__ AcceptSmem s;
   __shared__ WriterTable wt;
@@ -381,9 +641,13 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(FinishArgs a, const __
       if (n == 0) a.loaded[b] = 0u;
     }
   }
-  block_accept(tree, s);
+  if (SAMPLE)
+    block_accept_sampled<LT>(tree, s, a.sa, b, a.V, a.status);
+  else
+    block_accept(tree, s);
   const int acc = s.acc_len;
   if (part == 0) {
+    if (SAMPLE) block_draw_residual<LT>(tree, s, a.sa, b, a.V);
     write_accept_outputs(tree, s, b, a.acc_len, a.path, a.committed, nullptr);
     T *Mb = (T *)a.M + (long long)b * a.V * K;
     // writers: every node, or the accepted path (all top-K rows are in ids_s)
@@ -575,13 +839,38 @@ static size_t step_topk_ws(const tr_step_args *a) {
 
 static size_t step_counters_bytes(int B) { return tr_align_up((size_t)B * 4, 256); }
 
+static size_t step_stash_bytes(const tr_step_args *a) { return tr_align_up((size_t)a->B * a->tree->dev.N * 4, 256); }
+
 extern "C" size_t tr_step_workspace_bytes(const tr_step_args *a) {
   if (!a || !a->tree || a->B < 1) return 0;
-  return step_topk_ws(a) + 2 * step_counters_bytes(a->B) +
-         tr_align_up((size_t)a->B * a->tree->dev.N * 4, 256);
+  // + the rows' softmax statistics of tr_step_sampled
+  return step_topk_ws(a) + 2 * step_counters_bytes(a->B) + step_stash_bytes(a) +
+         tr_align_up((size_t)a->B * a->tree->dev.N * 8, 256);
 }
 
-extern "C" int tr_step(const tr_step_args *a, tr_stream_t stream) {
+template <typename T>
+static void launch_finish(const FinishArgs &f, const TreeDev &tree, dim3 grid, cudaStream_t s, bool sample,
+                          tr_ftype ltype) {
+  if (!sample)
+    finish_kernel<T, float, false><<<grid, kThreads, 0, s>>>(f, tree);
+  else if (ltype == TR_F32)
+    finish_kernel<T, float, true><<<grid, kThreads, 0, s>>>(f, tree);
+  else
+    finish_kernel<T, __nv_bfloat16, true><<<grid, kThreads, 0, s>>>(f, tree);
+}
+
+static int step_impl(const tr_step_args *a, float temperature, const float *U, tr_stream_t stream);
+
+extern "C" int tr_step(const tr_step_args *a, tr_stream_t stream) { return step_impl(a, 0.f, nullptr, stream); }
+
+extern "C" int tr_step_sampled(const tr_step_args *a, float temperature, const float *U, tr_stream_t stream) {
+  if (!U || !(temperature > 0.f) || !(temperature < INFINITY)) return TR_E_INVAL;
+  if (a && !a->logits) return TR_E_UNSUPPORTED;  // the draw reads the logits: not with the fused LM head
+  return step_impl(a, temperature, U, stream);
+}
+
+static int step_impl(const tr_step_args *a, float temperature, const float *U, tr_stream_t stream) {
+  const bool sample = U != nullptr;
   if (!a || !a->tree || !a->M || !a->tree_tok || !a->ids || !a->root || !a->L) return TR_E_INVAL;
   if (a->B < 1 || a->V < 1 || a->K != a->tree->dev.K) return TR_E_INVAL;
   if (a->mtype != TR_I32 && a->mtype != TR_I64) return TR_E_INVAL;
@@ -599,7 +888,12 @@ extern "C" int tr_step(const tr_step_args *a, tr_stream_t stream) {
   const TreeDev &tree = a->tree->dev;
   const int64_t rows = (int64_t)a->B * tree.N;
   const size_t tk_ws = step_topk_ws(a);
-  if (a->logits)
+  const size_t cnt_bytes = step_counters_bytes(a->B);
+  float2 *stats = (float2 *)((char *)a->ws + tk_ws + 2 * cnt_bytes + step_stash_bytes(a));
+  if (sample)
+    rc = tr_topk_softmax(a->logits, a->ltype, rows, a->V, a->ld, a->K, temperature, a->ids, a->vals, (float *)stats,
+                         a->ws, tk_ws, stream);
+  else if (a->logits)
     rc = tr_topk(a->logits, a->ltype, rows, a->V, a->ld, a->K, a->ids, a->vals, a->ws, tk_ws, stream);
   else
     rc = tr_lmhead_topk(a->H, a->Wt, rows, a->D, a->V, a->K, a->ids, a->vals, a->ws, tk_ws, stream);
@@ -625,14 +919,51 @@ extern "C" int tr_step(const tr_step_args *a, tr_stream_t stream) {
   f.heads_per_cta = commit ? commit_heads_per_cta(a->Hkv) : 1;
   f.mode = a->mode;
   f.counters = (unsigned *)((char *)a->ws + tk_ws);
-  f.loaded = (unsigned *)((char *)a->ws + tk_ws + step_counters_bytes(a->B));
-  f.stash = (int32_t *)((char *)a->ws + tk_ws + 2 * step_counters_bytes(a->B));
+  f.loaded = (unsigned *)((char *)a->ws + tk_ws + cnt_bytes);
+  f.stash = (int32_t *)((char *)a->ws + tk_ws + 2 * cnt_bytes);
   f.status = tr_status_dev();
+  f.sa.logits = a->logits;
+  f.sa.ld = a->ld;
+  f.sa.stats = stats;
+  f.sa.U = U;
+  f.sa.K1 = a->K + 1;
+  f.sa.c = sample ? 1.4426950408889634f / temperature : 0.f;
   const int G = commit ? (a->Hkv + f.heads_per_cta - 1) / f.heads_per_cta : 0;  // commit CTAs per sequence
+  const dim3 grid(a->B, 1 + G);
   if (a->mtype == TR_I64)
-    finish_kernel<long long><<<dim3(a->B, 1 + G), kThreads, 0, s>>>(f, tree);
+    launch_finish<long long>(f, tree, grid, s, sample, a->ltype);
   else
-    finish_kernel<int32_t><<<dim3(a->B, 1 + G), kThreads, 0, s>>>(f, tree);
+    launch_finish<int32_t>(f, tree, grid, s, sample, a->ltype);
+  TR_LAUNCH_CHECK();
+  return TR_OK;
+}
+
+extern "C" int tr_accept_sampled(const struct tr_tree *tree, int B, const int32_t *tree_tok, const int32_t *ids,
+                                 int K, const void *logits, tr_ftype ltype, int64_t V, int64_t ld, const float *stats,
+                                 float temperature, const float *U, int32_t *acc_len, int32_t *path,
+                                 int32_t *committed, int32_t *bonus, tr_stream_t stream) {
+  if (!tree || !tree_tok || !ids || !logits || !stats || !U || B < 1 || K < 1 || K > TR_MAX_K) return TR_E_INVAL;
+  if (K != tree->dev.K || V < 1 || ld < V || (ltype != TR_F32 && ltype != TR_BF16)) return TR_E_INVAL;
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return TR_E_INVAL;
+  if (V > INT32_MAX) return TR_E_UNSUPPORTED;
+  const size_t esz = ltype == TR_F32 ? 4 : 2;
+  if ((uintptr_t)logits % 16 || (ld * (int64_t)esz) % 16) return TR_E_UNSUPPORTED;
+  int rc = tr_check_device();
+  if (rc != TR_OK) return rc;
+  SampleArgs sa;
+  sa.logits = logits;
+  sa.ld = ld;
+  sa.stats = (const float2 *)stats;
+  sa.U = U;
+  sa.K1 = K + 1;
+  sa.c = 1.4426950408889634f / temperature;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (ltype == TR_F32)
+    accept_sampled_kernel<float><<<B, kThreads, 0, s>>>(tree->dev, tree_tok, ids, K, V, sa, acc_len, path, committed,
+                                                        bonus, tr_status_dev());
+  else
+    accept_sampled_kernel<__nv_bfloat16><<<B, kThreads, 0, s>>>(tree->dev, tree_tok, ids, K, V, sa, acc_len, path,
+                                                                committed, bonus, tr_status_dev());
   TR_LAUNCH_CHECK();
   return TR_OK;
 }

@@ -8,7 +8,7 @@ namespace {
 constexpr unsigned long long kGamma = 0x9E3779B97F4A7C15ull;
 enum {
   TAG_NEXT = 1, TAG_ALT = 2, TAG_NOISE = 3, TAG_WARM = 5, TAG_H = 12, TAG_W = 13, TAG_CLASS = 14, TAG_E = 15,
-  TAG_G = 16
+  TAG_G = 16, TAG_U = 17
 };
 constexpr int kAlt = 7;
 constexpr int kClasses = 16;
@@ -167,7 +167,26 @@ __global__ void warm_kernel(unsigned long long seed, int B, long long V, int K, 
   }
 }
 
+// out[(b*N + n)*K1 + j] = top 24 bits of output j of the stream at key (seed, 17, step, b, n), times 2^-24
+__global__ void uniforms_kernel(unsigned long long seed, long long step, int N, int K1, long long total, float *out) {
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const unsigned long long j = (unsigned long long)(e % K1), bn = (unsigned long long)(e / K1);
+    const unsigned long long key = hkey5(seed, TAG_U, (unsigned long long)step, bn / N, bn % N);
+    out[e] = (float)(mix64(key + kGamma * (j + 1ull)) >> 40) * (1.0f / 16777216.0f);
+  }
+}
+
 }  // namespace
+
+extern "C" int trsyn_uniforms(uint64_t seed, int64_t step, int B, int N, int K1, float *out, tr_stream_t stream) {
+  if (!out || B < 1 || N < 1 || K1 < 1) return TR_E_INVAL;
+  int rc = tr_check_device();
+  if (rc != TR_OK) return rc;
+  uniforms_kernel<<<tr_sm_count() * 2, 256, 0, (cudaStream_t)stream>>>(seed, step, N, K1, (long long)B * N * K1, out);
+  TR_LAUNCH_CHECK();
+  return TR_OK;
+}
 
 extern "C" int trsyn_logits(uint64_t seed, int B, int64_t V, const struct tr_tree *tree, const int32_t *tree_tok,
                             const int32_t *L, tr_ftype ftype, void *out, int64_t ld, tr_stream_t stream) {

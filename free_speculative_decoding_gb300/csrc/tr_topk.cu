@@ -181,7 +181,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   if (u0 >= u1) return;  // warps work alone: no block-wide barrier follows
 
   constexpr int kV = Elem<T>::kVec;
-  constexpr int kN = kVecs * kV;  // elements of a lane per step
   const long long row_bytes = V * (long long)sizeof(T);
   const int n_steps = (int)(u1 - u0);
 

@@ -17,7 +17,8 @@ from __future__ import annotations
 import torch
 
 from . import (TR_INIT_INHERIT, TR_UPD_ALL, Tree, make_step_args, tr_get_status, tr_init_matrix, tr_retrieve,
-               tr_step, tr_step_workspace_bytes, tr_verify_attn, tr_verify_attn_workspace_bytes, workspace)
+               tr_step, tr_step_sampled, tr_step_workspace_bytes, tr_verify_attn, tr_verify_attn_workspace_bytes,
+               workspace)
 
 
 class TRState:
@@ -73,14 +74,18 @@ class TRState:
         tr_verify_attn(Q, Kt, Vt, self.Kc, self.Vc, self.L, self.tree, self.O, self.scale, self.ws_attn)
         return self.O
 
-    def finish(self, logits=None, H=None, Wt=None, Kt=None, Vt=None, mode=TR_UPD_ALL):
-        """Everything after the target's forward pass: tr_step."""
+    def finish(self, logits=None, H=None, Wt=None, Kt=None, Vt=None, mode=TR_UPD_ALL, temperature=None, U=None):
+        """Everything after the target's forward pass: tr_step, or tr_step_sampled
+        at ``temperature`` with the uniforms U [B, N, K+1]."""
         a = make_step_args(self.tree, self.M, self.tree_tok, self.ids, self.vals, self.acc_len, self.path,
                            self.committed, self.root, self.L, logits=logits, H=H, Wt=Wt,
                            Kt=Kt if self.attention else None, Vt=Vt if self.attention else None,
                            Kc=self.Kc if self.attention else None, Vc=self.Vc if self.attention else None,
                            mode=mode, ws=self.ws_step)
-        tr_step(a)
+        if temperature is None:
+            tr_step(a)
+        else:
+            tr_step_sampled(a, temperature, U)
 
     def status(self):
         return tr_get_status()

@@ -178,6 +178,19 @@ int tr_topk(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t
             int32_t *ids, float *vals, void *ws, size_t ws_bytes, tr_stream_t stream);
 size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K);
 
+/* tr_topk plus each row's softmax statistics at temperature T, for acceptance
+ * under sampling (speculative-decoding lesson, the acceptance rule, which
+ * needs the target's probabilities p = softmax(x / T)): in the same single
+ * read of the logits, stats[r, 0] = max_v x[r, v] and
+ * stats[r, 1] = sum_v exp((x[r, v] - stats[r, 0]) / T), in fp32 (exp2 of the
+ * fp32-scaled difference, the sum in fp32: relative error ~1e-6).
+ *   stats [rows, 2] fp32 output; temperature positive and finite.
+ * logits and ld * element size must be 16-byte aligned (TR_E_UNSUPPORTED
+ * otherwise).  ws: tr_topk_workspace_bytes(rows, V, K) bytes, zeroed once. */
+int tr_topk_softmax(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K,
+                    float temperature, int32_t *ids, float *vals, float *stats, void *ws, size_t ws_bytes,
+                    tr_stream_t stream);
+
 /* Allocation-free variant of tr_topk (the paper has no counterpart; this is a
  * library convenience).  For callers that hold logits, ids and vals on the
  * device but cannot get more device memory: a plugin whose host framework owns
@@ -229,6 +242,32 @@ size_t tr_lmhead_topk_workspace_bytes(int64_t rows, int D, int64_t V, int K);
  *            tr_retrieve).  D = the tree's max depth. */
 int tr_accept(const struct tr_tree *tree, int B, const int32_t *tree_tok, const int32_t *ids, int K,
               int32_t *acc_len, int32_t *path, int32_t *committed, int32_t *bonus, tr_stream_t stream);
+
+/* Acceptance under sampling at temperature T.  The speculative-decoding
+ * lesson's rule (accept a drafted x with probability min(1, p(x) / q(x));
+ * on a rejection resample from norm(max(0, p - q))) applied to Token
+ * Recycling's tree, whose children are deterministic (q one-hot on the child's
+ * token; the hyper.ai summary, "Experiment", reports the method stays
+ * effective under sampling but gives no rule for the tree): starting at the
+ * root, the children of the current node are tried in rank order, child x
+ * being accepted when U[b, n, i] < r(x), where r is the node's p =
+ * softmax(logits / T) with the tokens of the siblings already rejected
+ * removed and renormalised; the walk moves to an accepted child and stops at
+ * a node n* whose children are all rejected (or a leaf).  The token committed
+ * after the path is the inverse CDF of n*'s residual r at U[b, n*, K] over
+ * token IDs in ascending order (the smallest y with r(0) + ... + r(y) > U).
+ * As T -> 0 this is the greedy rule of tr_accept.
+ *   tree_tok [B, N] int32; ids [B, N, K] int32 (the top-K; only a fallback
+ *   when n*'s residual has no weight left); logits [B*N, ld] of ltype with
+ *   16-byte aligned rows; stats [B*N, 2] from tr_topk_softmax at the same T;
+ *   U [B, N, K+1] fp32 uniforms in [0, 1) (the random numbers are inputs);
+ *   outputs as in tr_accept (bonus = the drawn token).
+ * fp32 arithmetic: a decision whose uniform lies within ~1e-6 of its
+ * threshold may differ from exact arithmetic. */
+int tr_accept_sampled(const struct tr_tree *tree, int B, const int32_t *tree_tok, const int32_t *ids, int K,
+                      const void *logits, tr_ftype ltype, int64_t V, int64_t ld, const float *stats,
+                      float temperature, const float *U, int32_t *acc_len, int32_t *path, int32_t *committed,
+                      int32_t *bonus, tr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* 5. Matrix update                                                           */
@@ -307,6 +346,15 @@ typedef struct tr_step_args {
 
 int tr_step(const tr_step_args *args, tr_stream_t stream);
 size_t tr_step_workspace_bytes(const tr_step_args *args);
+
+/* tr_step with the acceptance of tr_accept_sampled at temperature T: the
+ * top-K also yields each row's softmax statistics (tr_topk_softmax), the walk
+ * and the draw run in the fused step end, and the drawn token becomes the
+ * next root.  The matrix update (the top-K of every verified node) and the
+ * KV commit are those of tr_step.  U [B, N, K+1] fp32 uniforms on the device.
+ * Logits only (TR_E_UNSUPPORTED with the fused LM head, whose logits are never
+ * stored), 16-byte aligned rows; the same workspace as tr_step. */
+int tr_step_sampled(const tr_step_args *args, float temperature, const float *U, tr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Status and workspace                                                       */

@@ -53,6 +53,11 @@ int trsyn_lm_weight(uint64_t seed, int64_t V, int D, void *out, tr_stream_t stre
  * the Markov successor and alternates of t, the others uniform random IDs. */
 int trsyn_warm_matrix(uint64_t seed, int B, int64_t V, int K, tr_itype mtype, void *M, tr_stream_t stream);
 
+/* Uniforms for acceptance under sampling, out [B, N, K1] fp32: entry
+ * (b, n, j) is the top 24 bits of output j of the stream at key
+ * (seed, 17, step, b, n), times 2^-24 (exact in fp32). */
+int trsyn_uniforms(uint64_t seed, int64_t step, int B, int N, int K1, float *out, tr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

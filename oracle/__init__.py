@@ -36,7 +36,7 @@ from .tree import TreePlan
 from .tr import (
     INIT_ZERO, INIT_RANDOM, INIT_INHERIT, UPD_ALL, UPD_ACCEPTED,
     init_matrix, retrieve, tree_attention, topk, topk_rows, accept, update,
-    kv_commit, lmhead_logits, mix64_stream, softmax_stats, target_probs, accept_sampled,
+    kv_commit, lmhead_logits, mix64_stream, softmax_stats, target_probs, accept_sampled, draw_is_valid,
 )
 from .loop import TRState, tr_loop, greedy_decode
 
@@ -44,5 +44,5 @@ __all__ = [
     "TreePlan", "INIT_ZERO", "INIT_RANDOM", "INIT_INHERIT", "UPD_ALL", "UPD_ACCEPTED",
     "init_matrix", "retrieve", "tree_attention", "topk", "topk_rows", "accept", "update",
     "kv_commit", "lmhead_logits", "mix64_stream", "softmax_stats", "target_probs", "accept_sampled",
-    "TRState", "tr_loop", "greedy_decode",
+    "draw_is_valid", "TRState", "tr_loop", "greedy_decode",
 ]

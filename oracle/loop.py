@@ -59,8 +59,9 @@ def tr_loop(plan, states, target, steps, K, mode=UPD_ALL, qkv=None, scale=None,
             if temperature is None:
                 acc_len, path, committed, bonus = accept(plan, tok, ids[:, 0])
             else:
-                acc_len, path, committed, bonus, rec["margin"] = accept_sampled(
+                acc_len, path, committed, bonus, rec["margins"], rec["cdf"] = accept_sampled(
                     plan, tok, rows, temperature, uniforms(s, b))
+                rec["u_draw"] = float(uniforms(s, b)[path[-1], -1])
             update(st.M, tok, ids, plan, mode, path)
             if q is not None:
                 st.L = kv_commit(st.kc, st.vc, kt[i], vt[i], st.L, path)

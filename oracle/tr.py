@@ -200,11 +200,12 @@ def accept_sampled(plan, tok, logits, T, U):
     token IDs in ascending order (the smallest v with r(0) + ... + r(v) >
     U[n*, K]).  logits [N, V]: the target's logits at every node.
 
-    Returns (acc_len, path, committed, bonus, margin): margin is the smallest
-    distance between a uniform and the threshold it was compared with (for
-    the draw, the distance of U[n*, K] to the CDF at the chosen token and at
-    the one before it), so a caller can tell a decision that fp32 arithmetic
-    could flip."""
+    Returns (acc_len, path, committed, bonus, margins, cdf): margins =
+    (smallest distance between a child test's uniform and its threshold,
+    distance of U[n*, K] to the nearer end of the drawn token's CDF interval),
+    so a caller can tell a decision that fp32 arithmetic could flip; cdf is the
+    residual's CDF at n* (the tokens whose interval lies within a tolerance of
+    U[n*, K] are the draws such arithmetic can make)."""
     K1 = np.asarray(U).shape[1]
     n, path, margin = 0, [0], np.inf
     while True:
@@ -228,9 +229,16 @@ def accept_sampled(plan, tok, logits, T, U):
     y = int(np.searchsorted(cdf, u, side="right"))
     if y >= len(r):                          # rounding left the total just below u
         y = int(np.nonzero(r > 0)[0][-1])
-    margin = min(margin, abs(cdf[y] - u), abs(u - (cdf[y - 1] if y > 0 else 0.0)))
+    draw_margin = min(abs(cdf[y] - u), abs(u - (cdf[y - 1] if y > 0 else 0.0)))
     committed = [int(tok[m]) for m in path[1:]] + [y]
-    return plan.depth[n], path, committed, y, margin
+    return plan.depth[n], path, committed, y, (margin, draw_margin), cdf
+
+
+def draw_is_valid(cdf, u, y, tol):
+    """True when token y's interval [cdf(y-1), cdf(y)) of a residual CDF lies
+    within tol of u: a draw that arithmetic with error below tol can make."""
+    lo = cdf[y - 1] if y > 0 else 0.0
+    return cdf[y] > lo and lo - tol <= u < cdf[y] + tol
 
 
 def update(M, tok, ids, plan, mode=UPD_ALL, path=None):

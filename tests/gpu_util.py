@@ -106,13 +106,22 @@ def gpu_start(w, st, init="warm"):
         raise ValueError(init)
 
 
+U_SEED = 0xACC_E97      # seed of the acceptance uniforms in the sampling tests
+
+
+def oracle_uniforms(w, N):
+    return lambda step, b: synth.uniforms(U_SEED, step, b, N, w.K + 1)
+
+
 def run_gpu_loop(w, steps, record=True, keep_M_every=1, o_seqs=None, o_steps=None, device="cuda",
-                 init="warm", mode=0):
+                 init="warm", mode=0, temperature=None):
     """Run `steps` Token Recycling steps of workload w on the GPU; return per-step records.
 
     Attention outputs are kept for the sequences ``o_seqs`` at the steps
     ``o_steps`` (all by default).  ``init`` picks the starting matrices
-    (gpu_start), ``mode`` the update rule (TR_UPD_ALL or TR_UPD_ACCEPTED)."""
+    (gpu_start), ``mode`` the update rule (TR_UPD_ALL or TR_UPD_ACCEPTED).
+    With ``temperature`` every step is tr_step_sampled with the uniforms of
+    trsyn_uniforms(U_SEED, step)."""
     import free_speculative_decoding_gb300 as tr
     from free_speculative_decoding_gb300.engine import TRState
     from synth import device as sd
@@ -127,6 +136,7 @@ def run_gpu_loop(w, steps, record=True, keep_M_every=1, o_seqs=None, o_steps=Non
     if w.attention:
         sd.fill_cache(w, st)
     gpu_start(w, st, init)
+    U = torch.empty(w.B, tree.N, w.K + 1, dtype=torch.float32, device=device) if temperature else None
     recs = []
     for s in range(steps):
         rec = {"tok": st.tree_tok.cpu().numpy().copy(), "L": st.L.cpu().numpy().copy()}
@@ -140,6 +150,9 @@ def run_gpu_loop(w, steps, record=True, keep_M_every=1, o_seqs=None, o_steps=Non
                 rec["O_seqs"] = list(range(w.B)) if o_seqs is None else list(o_seqs)
         if w.logits == "lmhead":
             st.finish(H=tgt.hidden_for(st), Wt=tgt.Wt, Kt=kt, Vt=vt, mode=mode)
+        elif temperature:
+            tr.trsyn_uniforms(U_SEED, s, U)
+            st.finish(logits=tgt.logits_for(st), Kt=kt, Vt=vt, mode=mode, temperature=temperature, U=U)
         else:
             st.finish(logits=tgt.logits_for(st), Kt=kt, Vt=vt, mode=mode)
         if record:

@@ -45,11 +45,22 @@ def test_reference_line(workload, tree):
     one = cb["one_core"]
     assert one["cores"] == 1 and one["value"] > 0
     # the same workload description the GPU arm prints
-    ns = types.SimpleNamespace(workload=workload, tree=tree)
+    ns = types.SimpleNamespace(workload=workload, tree=tree, temperature=None, init="inherit", update="all")
     w = bench.workload_of(ns)
     assert d["config"] == bench.config_of(ns, w, 1)
     assert d["unit"] == "steps/s (%d sequences x %d-node tree per step)" % (w.B, w.N)
     assert d["config"]["tree"] == (tree or synth.WORKLOADS[workload].tree)
+
+
+def test_reference_line_sampling_and_ablation():
+    """Under sampling, and with a random start and accepted-only updates, the
+    oracle arm runs the same rule and names it in the shared config."""
+    lines = _run(None, "--workload", "tiny", "--steps", "1", "--warmup", "1", "--temperature", "0.5",
+                 "--init", "random", "--update", "accepted")
+    d = json.loads(lines[0])
+    assert d["config"]["acceptance"] == "sampled at T=0.5"
+    assert d["config"]["init"] == "random" and d["config"]["update"] == "accepted"
+    assert d["value"] > 0
 
 
 def test_reference_other_ranks_are_silent():

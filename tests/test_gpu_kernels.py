@@ -406,6 +406,7 @@ def test_attention_matches_oracle(tr, tree_name, B, Hq, Hkv, lens, cap):
             ref = oracle.tree_attention(q[b].float().numpy(), kc[b].float().numpy(), vc[b].float().numpy(),
                                         int(lens[b]), kt[b].float().numpy(), vt[b].float().numpy(), plan, scale)
             err = rows_rel_err(Og[b], ref)
+            print("attention %s B=%d Hq=%d Hkv=%d L=%d: max row rel err %.2e" % (tree_name, B, Hq, Hkv, lens[b], err))
             assert err <= ATTN_TOL, err
     _status_ok(tr)
 

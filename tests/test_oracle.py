@@ -512,15 +512,20 @@ def test_sampled_acceptance_hand_case():
     logits = np.log(np.array([[.1, .2, .3, .4], [.25, .25, .25, .25], [.7, .1, .1, .1]]))
     U = np.zeros((3, 5))
     U[0, 0], U[0, 1], U[2, 4] = 0.5, 0.3, 0.05
-    acc, path, com, bonus, _ = oracle.accept_sampled(plan, tok, logits, 1.0, U)
+    acc, path, com, bonus, _, _ = oracle.accept_sampled(plan, tok, logits, 1.0, U)
     assert (acc, path, com, bonus) == (1, [0, 2], [1, 0], 0)
     U[2, 4] = 0.75
     assert oracle.accept_sampled(plan, tok, logits, 1.0, U)[2] == [1, 1]
-    # both children rejected (.5 >= .4, .4 >= 1/3): draw from [1/6, 1/3, 1/2, 0] at U = .6 -> token 2
+    # both children rejected (.5 >= .4, then .4 >= 1/3): the residual without
+    # tokens 3 and 1 is [1/4, 0, 3/4, 0]; the draw at U = .6 gives token 2,
+    # whose interval [.25, 1) lies .35 from U at its nearer end
     U[0, 1], U[0, 4] = 0.4, 0.6
-    acc, path, com, bonus, margin = oracle.accept_sampled(plan, tok, logits, 1.0, U)
+    acc, path, com, bonus, margins, cdf = oracle.accept_sampled(plan, tok, logits, 1.0, U)
     assert (acc, path, com, bonus) == (0, [0], [2], 2)
-    assert abs(margin - min(0.1, 0.4 - 1 / 3, 0.6 - 0.5, 1.0 - 0.6)) < 1e-12
+    assert abs(margins[0] - (0.4 - 1 / 3)) < 1e-12 and abs(margins[1] - 0.35) < 1e-12
+    assert np.allclose(cdf, [0.25, 0.25, 1, 1])
+    assert oracle.draw_is_valid(cdf, 0.6, 2, 0.0) and not oracle.draw_is_valid(cdf, 0.6, 1, 0.05)
+    assert oracle.draw_is_valid(cdf, 0.26, 0, 0.05) and not oracle.draw_is_valid(cdf, 0.6, 3, 1.0)
 
 
 def _distinct_sibling_tokens(plan, V, rng):
