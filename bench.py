@@ -67,6 +67,7 @@ def config_of(args, wl, world):
             "tree_depth": wl.depth(), "prefix": list(wl.prefix), "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
             "acceptance": ("greedy" if args.temperature is None else "sampled at T=%g" % args.temperature),
             "init": args.init, "update": args.update,
+            **({"lm_operands": args.lm_operands} if wl.logits == "lmhead" else {}),
             "parallelism": "replicas (dp%d, no collective)" % world,
             "l2": ("every step reads its own recorded hidden rows; the weight (V x D bf16) is larger than L2"
                    if wl.logits == "lmhead" else
@@ -209,6 +210,13 @@ def run_gpu(args, rank, world):
     st = TRState(tree, w.B, w.V, m_dtype=mdt, Hq=w.Hq if w.attention else 0, Hkv=w.Hkv, d=w.d, cap=cap,
                  logits_dtype=ldt, D=w.D if lm else 0, device=dev)
     tgt = sd.DeviceTarget(w, tree, dev)
+    realistic = lm and args.lm_operands == "realistic"
+    if realistic:
+        # off-grid operands: the weight ~ N(0, 0.02^2) and every step's hidden
+        # rows ~ N(0, 1) in bf16, full mantissas (timing only: such a target
+        # does not depend on the tokens, so acceptance is incidental)
+        gen = torch.Generator(device=dev).manual_seed(w.seed)
+        tgt.Wt.copy_((torch.randn(w.V, w.D, generator=gen, device=dev) * 0.02).to(torch.bfloat16))
     if w.attention:
         sd.fill_cache(w, st)
     start_matrices(args, w, st)
@@ -249,7 +257,9 @@ def run_gpu(args, rank, world):
         s = gstep[0]
         if w.attention:
             sd.step_qkv(w, s, N, dev, out=(bufs["q"][i], bufs["kt"][i], bufs["vt"][i]))
-        if lm:
+        if realistic:
+            bufs["H"][i].copy_(torch.randn(w.B * N, w.D, generator=gen, device=dev).to(torch.bfloat16))
+        elif lm:
             tgt.hidden_for(st, bufs["H"][i])
         else:
             tgt.logits_for(st, bufs["logits"][i])
@@ -595,6 +605,9 @@ def main():
                     help="starting matrices: each sequence's inherited synthetic matrix, all zero, or random")
     ap.add_argument("--update", default="all", choices=["all", "accepted"],
                     help="matrix update from every verified node, or from the accepted path only")
+    ap.add_argument("--lm-operands", default="grid", choices=["grid", "realistic"],
+                    help="fused LM-head workload: the grid-valued synthetic target, or off-grid N(0,1) hidden "
+                         "rows and N(0, 0.02^2) weights (timing only)")
     args = ap.parse_args()
     if args.temperature is not None and synth.WORKLOADS[args.workload].logits == "lmhead":
         ap.error("sampling needs stored logits: not with the fused LM-head workload")

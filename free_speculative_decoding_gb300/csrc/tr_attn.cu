@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         tma_prefetch_desc(&tmVc);
         tma_prefetch_desc(&tmVt);
       }
+      const uint64_t kv_policy = l2_evict_first();  // the cache streams through once
       int cnt = 0, last[SMAX];
       for (int s = 0; s < SMAX; ++s) last[s] = -1;
       bool ok = true;
@@ -310,7 +311,8 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           uint8_t *dst = ring + s * C::KV_TILE;
           for (int half = 0; half < 2; ++half) {
             if (cache)
-              tma_load_2d(dst + half * C::KV_HALF, mc, &full[s], half * 64, (sg.b * a.Hkv + sg.g) * a.cap + j * BN);
+              tma_load_2d_hint(dst + half * C::KV_HALF, mc, &full[s], half * 64, (sg.b * a.Hkv + sg.g) * a.cap + j * BN,
+                               kv_policy);
             else
               tma_load_3d(dst + half * C::KV_HALF, mt, &full[s], half * 64, sg.g, sg.b * N + (j - sg.n_ct) * BN);
           }

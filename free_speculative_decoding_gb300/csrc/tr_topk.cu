@@ -250,12 +250,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     for (int q = 0; q < kStages; ++q) mbar_init(&ring.full[q], 1);
     fence_mbar_init();
   }
+  // the logits are read once: their lines go first, so the matrices the step
+  // end gathers from stay in L2
+  const uint64_t stream_policy = l2_evict_first();
   __syncwarp();
   auto issue = [&](int q) {
     const long long off = (long long)ic * kStep;
     const uint32_t bytes = (uint32_t)(min(row_bytes - off, (long long)kStep) & ~15ll);
     mbar_arrive_expect_tx(&ring.full[q], bytes);
-    if (bytes) bulk_load(ring.stage[q], base + ir * stride + off, bytes, &ring.full[q]);
+    if (bytes) bulk_load_hint(ring.stage[q], base + ir * stride + off, bytes, &ring.full[q], stream_policy);
     if (++ic == nch) {
       ic = 0;
       ++ir;

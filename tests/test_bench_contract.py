@@ -45,7 +45,8 @@ def test_reference_line(workload, tree):
     one = cb["one_core"]
     assert one["cores"] == 1 and one["value"] > 0
     # the same workload description the GPU arm prints
-    ns = types.SimpleNamespace(workload=workload, tree=tree, temperature=None, init="inherit", update="all")
+    ns = types.SimpleNamespace(workload=workload, tree=tree, temperature=None, init="inherit", update="all",
+                               lm_operands="grid")
     w = bench.workload_of(ns)
     assert d["config"] == bench.config_of(ns, w, 1)
     assert d["unit"] == "steps/s (%d sequences x %d-node tree per step)" % (w.B, w.N)
