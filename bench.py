@@ -150,6 +150,14 @@ def attn_bytes(w, N, L):
     return kv + tree + out
 
 
+def attn_flops(w, N, L):
+    """Algorithmic tensor work of one tr_verify_attn launch: Q.K^T and P.V over
+    every key a node's tile holds (the L_b cached keys and the N tree rows),
+    2 flops per multiply-add; the exponentials: one per (query head, node, key)."""
+    keys = int(np.sum(np.asarray(L, dtype=np.int64) + N))
+    return 4.0 * w.Hq * N * w.d * keys, float(w.Hq * N * keys)
+
+
 def launches_per_step(w):
     """libtr kernels launched by one timed step: verify attention (1), then
     tr_step = top-K (1) or fused LM head (tile + merge, 2), and the fused
@@ -308,6 +316,7 @@ def run_gpu(args, rank, world):
     total_ms = 0.0
     attn_ms, step_ms = [], []
     attn_bytes_list = []
+    attn_work = []
     done = 0
     replay_ok = True
     committed = 0
@@ -348,6 +357,7 @@ def run_gpu(args, rank, world):
             if w.attention:
                 attn_ms.append(evs[i][0].elapsed_time(evs[i][1]))
                 attn_bytes_list.append(attn_bytes(w, N, L_hist[i].cpu().numpy()))
+                attn_work.append(attn_flops(w, N, L_hist[i].cpu().numpy()))
             step_ms.append(evs[i][1].elapsed_time(evs[i][2]))
         replay_ok &= bool(torch.equal(st.M, ref_state[0]) and torch.equal(st.L, ref_state[1])
                           and torch.equal(st.root, ref_state[2]))
@@ -383,7 +393,8 @@ def run_gpu(args, rank, world):
 
     total_ms = max_over_ranks(total_ms, world, dev)
 
-    res = {"total_ms": total_ms, "attn_ms": attn_ms, "attn_bytes": attn_bytes_list, "replay_ok": replay_ok,
+    res = {"total_ms": total_ms, "attn_ms": attn_ms, "attn_bytes": attn_bytes_list, "attn_work": attn_work,
+           "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count, "replay_ok": replay_ok,
            "status": status, "clocks": clk, "committed": committed, "N": N, "w": w, "seg": seg,
            "step_ms": step_ms, "topk_ms": topk_ms}
 
@@ -669,9 +680,25 @@ def main():
         peak = float(peaks["hbm_gbs"])
         tr_ = TRAFFIC.get("attn")
         traffic = tr_["bytes"] if tr_ and tr_["sha"] == src_sha(*tr_["files"]) and args.workload == "batched" else None
-        roofline = {"kernel": "tr_verify_attn", "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                    "frac": ach / peak, "traffic": traffic, "peak_source": peak_kind,
-                    "algorithmic_bytes_per_launch": a_bytes, "ms_per_launch": a_ms}
+        flops, exps = (float(np.mean(x)) for x in zip(*res["attn_work"]))
+        tf = flops / (a_ms * 1e-3) / 1e12
+        # exp2 units: 16 per SM per clock (nominal), at the sampled SM clock
+        sm_mhz = res["clocks"].get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+        exp_peak = 16 * res["sm_count"] * sm_mhz * 1e6 / 1e9
+        exp_rate = exps / (a_ms * 1e-3) / 1e9
+        hbm = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak}
+        tensor = {"bound": "tensor", "achieved": tf, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
+                  "frac": tf / float(peaks["bf16_tflops"]), "flops_per_launch": flops}
+        exp = {"achieved": exp_rate, "peak": exp_peak, "unit": "Gexp2/s", "frac": exp_rate / exp_peak,
+               "peak_source": "16 exp2 per SM per clock x %d SMs x %.0f MHz (nominal unit count)"
+                              % (res["sm_count"], sm_mhz)}
+        # grouped-query heads read each K/V tile for several query heads: the
+        # tensor pipe, not HBM, is the bound there
+        main, other = (tensor, hbm) if wl.Hq != wl.Hkv else (hbm, tensor)
+        roofline = dict(kernel="tr_verify_attn", **main, traffic=traffic if main is hbm else None,
+                        peak_source=peak_kind + (" bf16 dense (burst)" if main is tensor else ""),
+                        algorithmic_bytes_per_launch=a_bytes, ms_per_launch=a_ms,
+                        **{"also_" + other["bound"]: other}, exp2=exp)
     if wl.logits == "lmhead" and res["step_ms"]:
         s_ms = float(np.mean(res["step_ms"]))
         flops = 2.0 * wl.B * N * wl.D * wl.V

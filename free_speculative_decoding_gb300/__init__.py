@@ -63,8 +63,9 @@ _SIGS = {
     "tr_topk": (_i, [_p, _i, _i64, _i64, _i64, _i, _p, _p, _p, _sz, _p]),
     "tr_topk_workspace_bytes": (_sz, [_i64, _i64, _i]),
     "tr_topk_noalloc": (_i, [_p, _i, _i64, _i64, _i64, _i, _p, _p, _p]),
-    "tr_topk_softmax": (_i, [_p, _i, _i64, _i64, _i64, _i, _f, _p, _p, _p, _p, _sz, _p]),
-    "tr_accept_sampled": (_i, [_p, _i, _p, _p, _i, _p, _i, _i64, _i64, _p, _f, _p, _p, _p, _p, _p, _p]),
+    "tr_topk_softmax": (_i, [_p, _i, _i64, _i64, _i64, _i, _f, _p, _p, _p, _p, _p, _sz, _p]),
+    "tr_softmax_steps": (_i, [_i64, _i]),
+    "tr_accept_sampled": (_i, [_p, _i, _p, _p, _i, _p, _i, _i64, _i64, _p, _p, _f, _p, _p, _p, _p, _p, _p]),
     "tr_step_sampled": (_i, [ctypes.POINTER(tr_step_args), _f, _p, _p]),
     "tr_lmhead_topk": (_i, [_p, _p, _i64, _i, _i64, _i, _p, _p, _p, _sz, _p]),
     "tr_lmhead_topk_workspace_bytes": (_sz, [_i64, _i, _i64, _i]),
@@ -248,28 +249,37 @@ def tr_topk_noalloc(logits, K, ids, vals, V=None):
                                                     _ptr(vals), _stream()))
 
 
-def tr_topk_softmax(logits, K, temperature, ids, vals, stats, ws, V=None):
-    """tr_topk plus stats [rows, 2] = (row max, sum of exp((x - max) / T))."""
+def tr_softmax_steps(V, dtype):
+    return lib().tr_softmax_steps(V, TR_F32 if dtype == torch.float32 else TR_BF16)
+
+
+def tr_topk_softmax(logits, K, temperature, ids, vals, stats, step_stats, ws, V=None):
+    """tr_topk plus stats [rows, 2] = (row max, sum of exp((x - max) / T)) and
+    step_stats [rows, tr_softmax_steps(V, dtype), 2], the same pair per 8 KB step."""
     rows, ld = logits.shape
     V = ld if V is None else V
     _i32(ids, "ids")
-    if stats.dtype != torch.float32:
+    if stats.dtype != torch.float32 or step_stats.dtype != torch.float32:
         raise ValueError("stats must be float32")
+    if step_stats.numel() < rows * tr_softmax_steps(V, logits.dtype) * 2:
+        raise ValueError("step_stats too small")
     _check("tr_topk_softmax", lib().tr_topk_softmax(_ptr(logits), _ftype(logits), rows, V, ld, K, float(temperature),
-                                                    _ptr(ids), _ptr(vals), _ptr(stats),
+                                                    _ptr(ids), _ptr(vals), _ptr(stats), _ptr(step_stats),
                                                     _ptr(ws) if ws is not None else None,
                                                     ws.numel() if ws is not None else 0, _stream()))
 
 
-def tr_accept_sampled(tree, tree_tok, ids, logits, stats, temperature, U, acc_len, path, committed, bonus, V=None):
+def tr_accept_sampled(tree, tree_tok, ids, logits, stats, step_stats, temperature, U, acc_len, path, committed,
+                      bonus, V=None):
     B = tree_tok.shape[0]
     K = ids.shape[-1]
     V = logits.shape[1] if V is None else V
-    if U.dtype != torch.float32 or stats.dtype != torch.float32:
-        raise ValueError("U and stats must be float32")
+    if U.dtype != torch.float32 or stats.dtype != torch.float32 or step_stats.dtype != torch.float32:
+        raise ValueError("U and the statistics must be float32")
     _check("tr_accept_sampled", lib().tr_accept_sampled(
         tree.handle, B, _ptr(tree_tok), _ptr(ids), K, _ptr(logits), _ftype(logits), V, logits.shape[1], _ptr(stats),
-        float(temperature), _ptr(U), _ptr(acc_len), _ptr(path), _ptr(committed), _ptr(bonus), _stream()))
+        _ptr(step_stats), float(temperature), _ptr(U), _ptr(acc_len), _ptr(path), _ptr(committed), _ptr(bonus),
+        _stream()))
 
 
 def tr_lmhead_topk_workspace_bytes(rows, D, V, K):

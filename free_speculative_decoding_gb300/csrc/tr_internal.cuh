@@ -89,7 +89,8 @@ static inline int tr_kmax(int K) { return K <= 8 ? 8 : (K <= 16 ? 16 : 32); }
 // top-K internals shared with the step and the LM head
 size_t tr_topk_counters_offset(int64_t rows, int64_t V, int K);  // byte offset of the arrival counters in the workspace
 // stats != NULL: also each row's (max, sum of exp((x - max) / temperature)) into stats [rows, 2]
+// and every 8 KB step's pair into step_stats [rows, tr_softmax_steps(V, ftype), 2]
 // (16-byte aligned rows only: the caller checks)
 int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K,
                    int32_t *ids, float *vals, void *ws, size_t ws_bytes, cudaStream_t stream,
-                   float temperature = 1.f, float *stats = nullptr);
+                   float temperature = 1.f, float *stats = nullptr, float *step_stats = nullptr);

@@ -71,6 +71,7 @@ struct AcceptSmem {
   int path[TR_MAX_NODES];
   float cw[TR_MAX_NODES];  // sampling: node n's weight 2^((x - max) c) in its parent's row
   float cz[TR_MAX_NODES];  // sampling: node n's normaliser Z (the same units)
+  float cu[TR_MAX_NODES];  // sampling: the uniform of node n's test, U[parent n, rank n]
   unsigned long long nomatch[2];
   int warp_best[kThreads / 32];
   int best;      // chosen node n*
@@ -208,6 +209,8 @@ struct SampleArgs {
   const void *logits;  // [B*N, ld] of the logit type
   long long ld;
   const float2 *stats; // [B*N] (row maximum, sum of 2^((x - max) c))
+  const float2 *sstats;// [B*N, nsteps] (step maximum, sum of 2^((x - step max) c)) per 8 KB step of a row
+  int nsteps;          // steps per row
   const float *U;      // [B, N, K1] uniforms in [0, 1)
   int K1;              // K + 1
   float c;             // log2(e) / temperature
@@ -231,6 +234,7 @@ __device__ void block_accept_sampled(const TreeDev &tree, AcceptSmem &s, const S
     s.cz[n] = sa.stats[rown].y;
     if (n > 0) {
       const long long rowp = (long long)b * N + tree.parent[n];
+      s.cu[n] = __ldg(sa.U + rowp * sa.K1 + tree.rank[n]);
       const int x = s.tok[n];
       float w = 0.f;
       if (x >= 0 && (long long)x < V) {
@@ -247,7 +251,6 @@ __device__ void block_accept_sampled(const TreeDev &tree, AcceptSmem &s, const S
     int cur = 0;
     while (true) {
       const int f = tree.child_first[cur], cnt = tree.child_count[cur];
-      const float *u = sa.U + ((long long)b * N + cur) * sa.K1;
       float rem = s.cz[cur];
       int next = -1;
       for (int i = 0; i < cnt; ++i) {
@@ -256,7 +259,7 @@ __device__ void block_accept_sampled(const TreeDev &tree, AcceptSmem &s, const S
         for (int j = 0; j < i; ++j) dup |= s.tok[f + j] == x;
         const float w = s.cw[ch];
         const float r = dup ? 0.f : w / fmaxf(rem, w);
-        if (__ldg(u + i) < r) {
+        if (s.cu[ch] < r) {
           next = ch;
           break;
         }
@@ -275,127 +278,159 @@ __device__ void block_accept_sampled(const TreeDev &tree, AcceptSmem &s, const S
 
 // The draw at the final node n*: the smallest token y with
 // r(0) + ... + r(y) > U[n*, K], r being n*'s distribution without its
-// (rejected) children's tokens.  Each thread sums the weights of a contiguous
-// chunk of the row (compensated fp32 sums), a block scan of the chunk sums in
-// fp64 finds the chunk where the running sum crosses U times the total, and
-// that chunk's thread walks it.  The weights' own fp32 rounding (~1e-6
-// relative) is then the only error of the running sum.  Loads go in batches of
-// whole 16-byte vectors (every chunk starts on one).  Returns y on every thread.
+// (rejected) children's tokens.  The top-K pass left a (maximum, sum) pair for
+// every 8 KB step of the row, so warp 0 scans those step sums (less the
+// rejected children's weights) in fp64 to find the step where the running sum
+// crosses U times the total; the block then loads that one step, coalesced,
+// each thread sums its slice of it, a block scan finds the slice, and its
+// thread walks the slice.  Returns y on every thread.
 template <typename LT>
 __device__ int block_draw_residual(const TreeDev &tree, AcceptSmem &s, const SampleArgs &sa, int b, long long V) {
-  constexpr int VW = Logit<LT>::kVec, BV = 8;  // elements per vector, vectors per batch
-  __shared__ double wsum[kThreads / 32 + 1];
+  constexpr int E = 8192 / (int)sizeof(LT);  // elements per step
+  constexpr int PER = E / kThreads;          // elements per thread of one step
+  constexpr int VW = Logit<LT>::kVec;
+  static_assert(PER % VW == 0, "whole vectors per thread");
+  __shared__ float rej_w[TR_MAX_K];   // weight of each rejected child's token (0 for a repeated token)
+  __shared__ int step_hit;            // the step the target falls in
+  __shared__ double step_base, target_s;
+  __shared__ float wpart[kThreads / 32];
   __shared__ int winner, last_pos;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, N = tree.N;
   const int nstar = s.best;
   const long long row = (long long)b * N + nstar;
   const LT *x = (const LT *)sa.logits + row * sa.ld;
-  const float mc = sa.stats[row].x * sa.c;
-  const float u = __ldg(sa.U + row * sa.K1 + (sa.K1 - 1));
+  const float M = sa.stats[row].x, mc = M * sa.c;
   const int f = tree.child_first[nstar], cnt = tree.child_count[nstar];
-  long long C = (V + kThreads - 1) / kThreads;
-  C = (C + VW - 1) / VW * VW;
-  const long long lo = min(V, (long long)t * C), hi = min(V, lo + C);
-  bool any_rej = false;  // does a rejected child's token fall in this chunk?
-  for (int i = 0; i < cnt; ++i) {
-    const int xr = s.tok[f + i];
-    any_rej |= xr >= lo && xr < hi;
+  if (t < cnt) {
+    const int xr = s.tok[f + t];
+    bool dup = xr < 0 || (long long)xr >= V;
+    for (int j = 0; j < t; ++j) dup |= s.tok[f + j] == xr;
+    rej_w[t] = dup ? 0.f : ex2_approx(fmaf(Logit<LT>::at(x + xr), sa.c, -mc));
   }
-  auto weight = [&](long long v, float l) -> float {
-    if (any_rej)
-      for (int i = 0; i < cnt; ++i)
-        if (s.tok[f + i] == v) return 0.f;
-    return ex2_approx(fmaf(l, sa.c, -mc));  // -inf (past the chunk) gives 0
-  };
-  auto load_batch = [&](long long v0, float (&e)[BV][VW]) {
-#pragma unroll
-    for (int j = 0; j < BV; ++j) {
-      const long long vj = v0 + j * VW;
-      if (vj + VW <= hi) {
-        Logit<LT>::vec(x + vj, e[j]);
-      } else {
-#pragma unroll
-        for (int q = 0; q < VW; ++q) e[j][q] = vj + q < hi ? Logit<LT>::at(x + vj + q) : -INFINITY;
-      }
-    }
-  };
-  // compensated (Kahan) running sum in fp32: sum - comp tracks the exact sum closely
-  struct Kahan {
-    float sum = 0.f, comp = 0.f;
-    __device__ __forceinline__ void add(float e) {
-      const float y = e - comp;
-      const float tt = sum + y;
-      comp = (tt - sum) - y;
-      sum = tt;
-    }
-    __device__ __forceinline__ double value() const { return (double)sum - (double)comp; }
-  };
-  // pass 1: the chunk's sum, element by element in token order
-  Kahan k1;
-  for (long long v0 = lo; v0 < hi; v0 += BV * VW) {
-    float e[BV][VW];
-    load_batch(v0, e);
-#pragma unroll
-    for (int j = 0; j < BV; ++j)
-#pragma unroll
-      for (int q = 0; q < VW; ++q) k1.add(weight(v0 + j * VW + q, e[j][q]));
-  }
-  const double z = k1.value();
-  // exclusive and inclusive prefix of the chunk sums (fp64): incl of thread t
-  // is bitwise the excl of thread t + 1, so the chunks' intervals tile [0, total)
-  double incl = z;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const double o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
-  }
-  const double excl_w = __shfl_up_sync(0xffffffffu, incl, 1);
   if (t == 0) {
     winner = -1;
     last_pos = -1;
   }
-  if (lane == 31) wsum[warp] = incl;
   __syncthreads();
-  if (t == 0) {
-    double acc = 0.0;
-    for (int w = 0; w < kThreads / 32; ++w) {
-      const double tw = wsum[w];
-      wsum[w] = acc;
-      acc += tw;
+  if (warp == 0) {
+    // the steps' weights in units of the row maximum, rejected tokens removed
+    const float2 *ss = sa.sstats + row * sa.nsteps;
+    auto step_w = [&](int st) -> double {
+      if (st >= sa.nsteps) return 0.0;
+      const float2 p = ss[st];
+      double w = p.y == 0.f ? 0.0 : (double)p.y * (double)ex2_approx((p.x - M) * sa.c);
+      for (int i = 0; i < cnt; ++i)
+        if (s.tok[f + i] / E == st) w -= (double)rej_w[i];
+      return w > 0.0 ? w : 0.0;
+    };
+    double total = 0.0;
+    for (int g = 0; g < sa.nsteps; g += 32) {
+      double w = step_w(g + lane);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) w += __shfl_xor_sync(0xffffffffu, w, off);
+      total += w;
     }
-    wsum[kThreads / 32] = acc;
+    const double target = (double)__ldg(sa.U + row * sa.K1 + (sa.K1 - 1)) * total;
+    double base = 0.0;
+    int hit = -1, last = -1;
+    for (int g = 0; g < sa.nsteps && hit < 0; g += 32) {
+      const double w = step_w(g + lane);
+      double incl = w;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const double o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const unsigned cross = __ballot_sync(0xffffffffu, w > 0.0 && base + incl > target);
+      const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0);
+      if (pos) last = g + 31 - __clz(pos);
+      if (cross) {
+        const int l = __ffs(cross) - 1;
+        hit = g + l;
+        base += __shfl_sync(0xffffffffu, incl - w, l);
+      } else {
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    if (lane == 0) {
+      if (hit < 0) {  // rounding left the total at or below the target: the last token with weight
+        hit = last;
+        base = -INFINITY;  // no slice claims the target, so the last slice with weight walks
+      }
+      step_hit = hit;
+      step_base = base;
+      target_s = target;
+    }
   }
   __syncthreads();
-  const double woff = wsum[warp];
-  const double total = wsum[kThreads / 32];
-  incl += woff;
-  const double excl = lane == 0 ? woff : excl_w + woff;
-  const double target = (double)u * total;
-  if (excl <= target && target < incl) winner = t;
-  if (z > 0.0) atomicMax(&last_pos, t);
-  __syncthreads();
-  // no chunk claims u * total only through rounding (u * total == total): the last chunk with weight
-  const int wt = winner >= 0 ? winner : last_pos;
-  if (t == 0 && wt < 0) s.bonus = s.top1[nstar];  // no weight left at all (the children held it all)
-  if (t == wt) {
-    // pass 2: the same compensated sum, element by element, until it passes the target
-    Kahan k2;
-    long long y = -1, last_tok = -1;
-    for (long long v0 = lo; v0 < hi && y < 0; v0 += BV * VW) {
-      float e[BV][VW];
-      load_batch(v0, e);
+  const int hit = step_hit;
+  if (hit < 0) {  // no weight left at all (the children held it all)
+    if (t == 0) s.bonus = s.top1[nstar];
+    __syncthreads();
+    return s.bonus;
+  }
+  // the step's elements, PER consecutive ones per thread
+  const long long e0 = (long long)hit * E + (long long)t * PER;
+  float w[PER];
 #pragma unroll
-      for (int j = 0; j < BV; ++j)
+  for (int v = 0; v < PER; v += VW) {
+    float e[VW];
+    if (e0 + v + VW <= V) {
+      Logit<LT>::vec(x + e0 + v, e);
+    } else {
 #pragma unroll
-        for (int q = 0; q < VW; ++q) {
-          const long long v = v0 + j * VW + q;
-          const float w = weight(v, e[j][q]);
-          if (w > 0.f) last_tok = v;
-          k2.add(w);
-          if (y < 0 && w > 0.f && excl + k2.value() > target) y = v;
-        }
+      for (int q = 0; q < VW; ++q) e[q] = e0 + v + q < V ? Logit<LT>::at(x + e0 + v + q) : -INFINITY;
     }
-    s.bonus = (int)(y >= 0 ? y : last_tok);
+#pragma unroll
+    for (int q = 0; q < VW; ++q) w[v + q] = ex2_approx(fmaf(e[q], sa.c, -mc));
+  }
+  for (int i = 0; i < cnt; ++i) {  // rejected children's tokens carry no weight
+    const long long o = (long long)s.tok[f + i] - e0;
+    if (o >= 0 && o < PER)
+#pragma unroll
+      for (int q = 0; q < PER; ++q)
+        if (q == o) w[q] = 0.f;
+  }
+  float z = 0.f;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) z += w[q];
+  // block scan of the slices' sums: incl of thread t is bitwise the excl of t + 1
+  float incl = z;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  const float excl_w = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 31) wpart[warp] = incl;
+  __syncthreads();
+  if (t == 0) {
+    float acc = 0.f;
+    for (int k = 0; k < kThreads / 32; ++k) {
+      const float tw = wpart[k];
+      wpart[k] = acc;
+      acc += tw;
+    }
+  }
+  __syncthreads();
+  const float woff = wpart[warp];
+  incl += woff;
+  const float excl = lane == 0 ? woff : excl_w + woff;
+  const float rel = (float)(target_s - step_base);  // the target inside the step
+  if (z > 0.f && excl <= rel && rel < incl) winner = t;
+  if (z > 0.f) atomicMax(&last_pos, t);
+  __syncthreads();
+  const int wt = winner >= 0 ? winner : last_pos;
+  if (t == wt) {
+    float acc = excl;
+    int y = -1, lastp = -1;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      if (w[q] > 0.f) lastp = q;
+      acc += w[q];
+      if (y < 0 && w[q] > 0.f && acc > rel) y = q;
+    }
+    s.bonus = (int)(e0 + (y >= 0 ? y : lastp));
   }
   __syncthreads();
   return s.bonus;
@@ -841,11 +876,18 @@ static size_t step_counters_bytes(int B) { return tr_align_up((size_t)B * 4, 256
 
 static size_t step_stash_bytes(const tr_step_args *a) { return tr_align_up((size_t)a->B * a->tree->dev.N * 4, 256); }
 
+static size_t step_stats_bytes(const tr_step_args *a) { return tr_align_up((size_t)a->B * a->tree->dev.N * 8, 256); }
+
+// per 8 KB step of every row (fp32 rows have the most steps)
+static size_t step_sstats_bytes(const tr_step_args *a) {
+  return tr_align_up((size_t)a->B * a->tree->dev.N * tr_softmax_steps(a->V, TR_F32) * 8, 256);
+}
+
 extern "C" size_t tr_step_workspace_bytes(const tr_step_args *a) {
   if (!a || !a->tree || a->B < 1) return 0;
-  // + the rows' softmax statistics of tr_step_sampled
-  return step_topk_ws(a) + 2 * step_counters_bytes(a->B) + step_stash_bytes(a) +
-         tr_align_up((size_t)a->B * a->tree->dev.N * 8, 256);
+  // + the rows' and their steps' softmax statistics of tr_step_sampled
+  return step_topk_ws(a) + 2 * step_counters_bytes(a->B) + step_stash_bytes(a) + step_stats_bytes(a) +
+         step_sstats_bytes(a);
 }
 
 template <typename T>
@@ -890,9 +932,10 @@ static int step_impl(const tr_step_args *a, float temperature, const float *U, t
   const size_t tk_ws = step_topk_ws(a);
   const size_t cnt_bytes = step_counters_bytes(a->B);
   float2 *stats = (float2 *)((char *)a->ws + tk_ws + 2 * cnt_bytes + step_stash_bytes(a));
+  float2 *sstats = (float2 *)((char *)stats + step_stats_bytes(a));
   if (sample)
     rc = tr_topk_softmax(a->logits, a->ltype, rows, a->V, a->ld, a->K, temperature, a->ids, a->vals, (float *)stats,
-                         a->ws, tk_ws, stream);
+                         (float *)sstats, a->ws, tk_ws, stream);
   else if (a->logits)
     rc = tr_topk(a->logits, a->ltype, rows, a->V, a->ld, a->K, a->ids, a->vals, a->ws, tk_ws, stream);
   else
@@ -925,6 +968,8 @@ static int step_impl(const tr_step_args *a, float temperature, const float *U, t
   f.sa.logits = a->logits;
   f.sa.ld = a->ld;
   f.sa.stats = stats;
+  f.sa.sstats = sstats;
+  f.sa.nsteps = tr_softmax_steps(a->V, a->ltype);
   f.sa.U = U;
   f.sa.K1 = a->K + 1;
   f.sa.c = sample ? 1.4426950408889634f / temperature : 0.f;
@@ -940,9 +985,10 @@ static int step_impl(const tr_step_args *a, float temperature, const float *U, t
 
 extern "C" int tr_accept_sampled(const struct tr_tree *tree, int B, const int32_t *tree_tok, const int32_t *ids,
                                  int K, const void *logits, tr_ftype ltype, int64_t V, int64_t ld, const float *stats,
-                                 float temperature, const float *U, int32_t *acc_len, int32_t *path,
-                                 int32_t *committed, int32_t *bonus, tr_stream_t stream) {
-  if (!tree || !tree_tok || !ids || !logits || !stats || !U || B < 1 || K < 1 || K > TR_MAX_K) return TR_E_INVAL;
+                                 const float *step_stats, float temperature, const float *U, int32_t *acc_len,
+                                 int32_t *path, int32_t *committed, int32_t *bonus, tr_stream_t stream) {
+  if (!tree || !tree_tok || !ids || !logits || !stats || !step_stats || !U || B < 1 || K < 1 || K > TR_MAX_K)
+    return TR_E_INVAL;
   if (K != tree->dev.K || V < 1 || ld < V || (ltype != TR_F32 && ltype != TR_BF16)) return TR_E_INVAL;
   if (!(temperature > 0.f) || !(temperature < INFINITY)) return TR_E_INVAL;
   if (V > INT32_MAX) return TR_E_UNSUPPORTED;
@@ -954,6 +1000,8 @@ extern "C" int tr_accept_sampled(const struct tr_tree *tree, int B, const int32_
   sa.logits = logits;
   sa.ld = ld;
   sa.stats = (const float2 *)stats;
+  sa.sstats = (const float2 *)step_stats;
+  sa.nsteps = tr_softmax_steps(V, ltype);
   sa.U = U;
   sa.K1 = K + 1;
   sa.c = 1.4426950408889634f / temperature;

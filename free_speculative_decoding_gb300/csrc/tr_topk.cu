@@ -160,16 +160,20 @@ __device__ __forceinline__ float2 warp_stats(float m, float z, float c) {
 }
 
 // STATS: also the row's softmax statistics at temperature T, c = log2(e) / T:
-// stats[row] = (max, sum of exp((x - max) / T)), from a running (max, sum) per
-// lane over the elements it examines (exp2 with the sum rescaled when the
-// lane's maximum grows), combined over the lanes at the end of a row segment
-// and, for a row split between warps, over the segments by the merging warp
+// stats[row] = (max, sum of exp((x - max) / T)), and the same pair for every
+// 8 KB step of the row, sstats[row * nch + step] = (step max, sum of
+// exp((x - step max) / T) over the step), from which a sampled token can be
+// located one step at a time.  Per step the warp takes the step's maximum,
+// each lane sums its elements' exp2 against it, and a warp sum gives the
+// step's pair; the lanes' running sums share one warp-wide running maximum
+// (rescaled when it grows), are summed at the end of a row segment and, for
+// a row split between warps, combined over the segments by the merging warp
 // (pstats holds one pair per list slot).
 template <typename T, int KMAX, bool STATS>
 __global__ void __launch_bounds__(kWarps * 32, 1)
     topk_warp_kernel(const T *__restrict__ x, long long V, long long ld, int K, int nch, long long U, int32_t *ids,
                      float *vals, unsigned long long *part, unsigned *counters, unsigned *status,
-                     unsigned long long wait_ns, float c, float2 *stats, float2 *pstats) {
+                     unsigned long long wait_ns, float c, float2 *stats, float2 *pstats, float2 *sstats) {
   using namespace sm100;
   extern __shared__ unsigned char smem_raw[];
   const int lane = threadIdx.x & 31;
@@ -318,22 +322,31 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       return m;
     };
     float lm = lane_max();
-    if (STATS && !isnan(lm)) {
-      // every element of the step enters the lane's running sum, before the
-      // top-K passes below clear any of them from the stage
-      const float nm = fmaxf(st_m, lm), nmc = nm * c;
-      float z4[4] = {st_m == -INFINITY ? 0.f : st_z * sm100::ex2((st_m - nm) * c), 0.f, 0.f, 0.f};
+    if (STATS) {
+      // every element of the step enters the sums, before the top-K passes
+      // below clear any of them from the stage
+      float sm = isnan(lm) ? -INFINITY : lm;  // the step's maximum (some lane holds an element)
+#pragma unroll
+      for (int off = 16; off; off >>= 1) sm = fmaxf(sm, __shfl_xor_sync(kFull, sm, off));
+      const float smc = sm * c;
+      float z4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < kVecs; ++j) {
         if (j * 32 + lane < nvec) {
           float e[kV];
           Elem<T>::unpack(sv[j * 32 + lane], e);
 #pragma unroll
-          for (int qq = 0; qq < kV; ++qq) z4[qq & 3] += sm100::ex2(fmaf(e[qq], c, -nmc));
+          for (int qq = 0; qq < kV; ++qq) z4[qq & 3] += sm100::ex2(fmaf(e[qq], c, -smc));
         }
       }
-      if (!isnan(tv)) z4[1] += sm100::ex2(fmaf(tv, c, -nmc));
-      st_z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+      if (!isnan(tv)) z4[1] += sm100::ex2(fmaf(tv, c, -smc));
+      const float zl = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+      float zs = zl;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) zs += __shfl_xor_sync(kFull, zs, off);
+      if (lane == 0) sstats[r * nch + cc] = make_float2(sm, zs);
+      const float nm = fmaxf(st_m, sm);  // warp-wide, so every rescale factor is at most 1
+      st_z = (st_m == -INFINITY ? 0.f : st_z * sm100::ex2((st_m - nm) * c)) + zl * sm100::ex2((sm - nm) * c);
       st_m = nm;
     }
     // An element enters only above the floor f: the K-th best value held,
@@ -535,7 +548,7 @@ size_t part_bytes_for(long long rows, long long V, int K) {
 template <typename T, int KMAX, bool STATS>
 cudaError_t launch_warp(const void *logits, long long rows, long long V, long long ld, int K, int32_t *ids,
                         float *vals, unsigned long long *part, unsigned *counters, float c, float2 *stats,
-                        float2 *pstats, cudaStream_t s) {
+                        float2 *pstats, float2 *sstats, cudaStream_t s) {
   const int nch = (int)steps_per_row(V, sizeof(T));
   const long long U = rows * nch;
   const long long want = (U + kWarps - 1) / kWarps;
@@ -552,7 +565,7 @@ cudaError_t launch_warp(const void *logits, long long rows, long long V, long lo
   }
   topk_warp_kernel<T, KMAX, STATS><<<grid, kWarps * 32, kRingSmem, s>>>(
       (const T *)logits, V, ld, K, nch, U, ids, vals, part, counters, tr_status_dev(), tr_wait_limit_ns(), c, stats,
-      pstats);
+      pstats, sstats);
   return cudaGetLastError();
 }
 
@@ -588,14 +601,16 @@ size_t pstats_bytes_for(long long rows, long long V) { return tr_align_up((size_
 
 template <typename T, int KMAX>
 cudaError_t launch(const void *logits, long long rows, long long V, long long ld, int K, int32_t *ids, float *vals,
-                   void *ws, float c, float2 *stats, cudaStream_t s) {
+                   void *ws, float c, float2 *stats, float2 *sstats, cudaStream_t s) {
   unsigned long long *part = (unsigned long long *)ws;
   unsigned *counters = (unsigned *)((char *)ws + (ws ? part_bytes_for(rows, V, K) : 0));
   float2 *pstats = (float2 *)((char *)ws + (ws ? part_bytes_for(rows, V, K) + counters_bytes_for(rows) : 0));
   const bool aligned = ((uintptr_t)logits % 16 == 0) && ((ld * (long long)sizeof(T)) % 16 == 0);
-  if (stats) return launch_warp<T, KMAX, true>(logits, rows, V, ld, K, ids, vals, part, counters, c, stats, pstats, s);
+  if (stats)
+    return launch_warp<T, KMAX, true>(logits, rows, V, ld, K, ids, vals, part, counters, c, stats, pstats, sstats, s);
   if (aligned)
-    return launch_warp<T, KMAX, false>(logits, rows, V, ld, K, ids, vals, part, counters, 0.f, nullptr, nullptr, s);
+    return launch_warp<T, KMAX, false>(logits, rows, V, ld, K, ids, vals, part, counters, 0.f, nullptr, nullptr,
+                                       nullptr, s);
   return launch_scan<T, KMAX>(logits, rows, V, ld, K, ids, vals, part, counters, s);
 }
 
@@ -610,11 +625,13 @@ extern "C" size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K) {
 size_t tr_topk_counters_offset(int64_t rows, int64_t V, int K) { return part_bytes_for(rows, V, K); }
 
 int tr_topk_launch(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K, int32_t *ids,
-                   float *vals, void *ws, size_t ws_bytes, cudaStream_t s, float temperature, float *stats) {
+                   float *vals, void *ws, size_t ws_bytes, cudaStream_t s, float temperature, float *stats,
+                   float *step_stats) {
   (void)ws_bytes;
   const int km = tr_kmax(K);
   const float c = stats ? 1.4426950408889634f / temperature : 0.f;
-#define TR_TOPK_CASE(T, KM) launch<T, KM>(logits, rows, V, ld, K, ids, vals, ws, c, (float2 *)stats, s)
+#define TR_TOPK_CASE(T, KM) \
+  launch<T, KM>(logits, rows, V, ld, K, ids, vals, ws, c, (float2 *)stats, (float2 *)step_stats, s)
   cudaError_t e;
   if (ftype == TR_F32)
     e = km == 8 ? TR_TOPK_CASE(float, 8) : km == 16 ? TR_TOPK_CASE(float, 16) : TR_TOPK_CASE(float, 32);
@@ -642,15 +659,20 @@ extern "C" int tr_topk(const void *logits, tr_ftype ftype, int64_t rows, int64_t
   return tr_topk_launch(logits, ftype, rows, V, ld, K, ids, vals, ws, ws_bytes, (cudaStream_t)stream);
 }
 
+extern "C" int tr_softmax_steps(int64_t V, tr_ftype ftype) {
+  if (V < 1 || (ftype != TR_F32 && ftype != TR_BF16)) return 0;
+  return (int)steps_per_row(V, ftype == TR_F32 ? 4 : 2);
+}
+
 extern "C" int tr_topk_softmax(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K,
-                               float temperature, int32_t *ids, float *vals, float *stats, void *ws, size_t ws_bytes,
-                               tr_stream_t stream) {
+                               float temperature, int32_t *ids, float *vals, float *stats, float *step_stats,
+                               void *ws, size_t ws_bytes, tr_stream_t stream) {
   if (rows < 0 || V < 1 || K < 1 || K > TR_MAX_K || K > V || ld < V) return TR_E_INVAL;
   if (ftype != TR_F32 && ftype != TR_BF16) return TR_E_INVAL;
   if (!(temperature > 0.f) || !(temperature < INFINITY)) return TR_E_INVAL;
   if (V > INT32_MAX) return TR_E_UNSUPPORTED;
   if (rows == 0) return TR_OK;
-  if (!logits || !ids || !stats) return TR_E_INVAL;
+  if (!logits || !ids || !stats || !step_stats) return TR_E_INVAL;
   const size_t esz = ftype == TR_F32 ? 4 : 2;
   if ((uintptr_t)logits % 16 || (ld * (int64_t)esz) % 16) return TR_E_UNSUPPORTED;  // streamed rows only
   const size_t need = tr_topk_workspace_bytes(rows, V, K);
@@ -658,5 +680,5 @@ extern "C" int tr_topk_softmax(const void *logits, tr_ftype ftype, int64_t rows,
   int rc = tr_check_device();
   if (rc != TR_OK) return rc;
   return tr_topk_launch(logits, ftype, rows, V, ld, K, ids, vals, ws, ws_bytes, (cudaStream_t)stream, temperature,
-                        stats);
+                        stats, step_stats);
 }

@@ -182,14 +182,21 @@ size_t tr_topk_workspace_bytes(int64_t rows, int64_t V, int K);
  * under sampling (speculative-decoding lesson, the acceptance rule, which
  * needs the target's probabilities p = softmax(x / T)): in the same single
  * read of the logits, stats[r, 0] = max_v x[r, v] and
- * stats[r, 1] = sum_v exp((x[r, v] - stats[r, 0]) / T), in fp32 (exp2 of the
- * fp32-scaled difference, the sum in fp32: relative error ~1e-6).
- *   stats [rows, 2] fp32 output; temperature positive and finite.
+ * stats[r, 1] = sum_v exp((x[r, v] - stats[r, 0]) / T), and the same pair
+ * for every 8 KB step of the row (2048 fp32 or 4096 bf16 entries; step s
+ * covers entries [s*E, (s+1)*E)): step_stats[r, s, 0] = the step's maximum,
+ * step_stats[r, s, 1] = sum over the step of exp((x - that maximum) / T).
+ * fp32 throughout (exp2 of the fp32-scaled difference): relative error
+ * ~1e-6.
+ *   stats [rows, 2], step_stats [rows, tr_softmax_steps(V, ftype), 2] fp32;
+ *   temperature positive and finite.
  * logits and ld * element size must be 16-byte aligned (TR_E_UNSUPPORTED
  * otherwise).  ws: tr_topk_workspace_bytes(rows, V, K) bytes, zeroed once. */
 int tr_topk_softmax(const void *logits, tr_ftype ftype, int64_t rows, int64_t V, int64_t ld, int K,
-                    float temperature, int32_t *ids, float *vals, float *stats, void *ws, size_t ws_bytes,
-                    tr_stream_t stream);
+                    float temperature, int32_t *ids, float *vals, float *stats, float *step_stats, void *ws,
+                    size_t ws_bytes, tr_stream_t stream);
+/* Steps per row of tr_topk_softmax's step_stats: ceil(V * element size / 8192). */
+int tr_softmax_steps(int64_t V, tr_ftype ftype);
 
 /* Allocation-free variant of tr_topk (the paper has no counterpart; this is a
  * library convenience).  For callers that hold logits, ids and vals on the
@@ -259,15 +266,16 @@ int tr_accept(const struct tr_tree *tree, int B, const int32_t *tree_tok, const 
  * As T -> 0 this is the greedy rule of tr_accept.
  *   tree_tok [B, N] int32; ids [B, N, K] int32 (the top-K; only a fallback
  *   when n*'s residual has no weight left); logits [B*N, ld] of ltype with
- *   16-byte aligned rows; stats [B*N, 2] from tr_topk_softmax at the same T;
- *   U [B, N, K+1] fp32 uniforms in [0, 1) (the random numbers are inputs);
- *   outputs as in tr_accept (bonus = the drawn token).
+ *   16-byte aligned rows; stats and step_stats from tr_topk_softmax at the
+ *   same T (the draw finds its step from the step sums, then reads that step
+ *   of n*'s row only); U [B, N, K+1] fp32 uniforms in [0, 1) (the random
+ *   numbers are inputs); outputs as in tr_accept (bonus = the drawn token).
  * fp32 arithmetic: a decision whose uniform lies within ~1e-6 of its
  * threshold may differ from exact arithmetic. */
 int tr_accept_sampled(const struct tr_tree *tree, int B, const int32_t *tree_tok, const int32_t *ids, int K,
                       const void *logits, tr_ftype ltype, int64_t V, int64_t ld, const float *stats,
-                      float temperature, const float *U, int32_t *acc_len, int32_t *path, int32_t *committed,
-                      int32_t *bonus, tr_stream_t stream);
+                      const float *step_stats, float temperature, const float *U, int32_t *acc_len,
+                      int32_t *path, int32_t *committed, int32_t *bonus, tr_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* 5. Matrix update                                                           */

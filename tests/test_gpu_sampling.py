@@ -71,17 +71,24 @@ def test_topk_softmax_statistics(tr, rows, V, K, dtype, T):
     ids = torch.zeros(rows, K, dtype=torch.int32, device="cuda")
     vals = torch.zeros(rows, K, dtype=torch.float32, device="cuda")
     stats = torch.zeros(rows, 2, dtype=torch.float32, device="cuda")
+    S = tr.tr_softmax_steps(V, dtype)
+    E = 8192 // (4 if dtype == torch.float32 else 2)
+    assert S == -(-V // E)
+    sstats = torch.zeros(rows, S, 2, dtype=torch.float32, device="cuda")
     ws = tr.workspace(tr.tr_topk_workspace_bytes(rows, V, K))
     ids_ref, vals_ref = oracle.topk_rows(xf, K)
     for _ in range(2):
-        tr.tr_topk_softmax(xd, K, T, ids, vals, stats, ws)
+        tr.tr_topk_softmax(xd, K, T, ids, vals, stats, sstats, ws)
         assert np.array_equal(ids.cpu().numpy(), ids_ref)
         assert np.array_equal(vals.cpu().numpy(), vals_ref.astype(np.float32))
-        st = stats.cpu().numpy()
+        st, sst = stats.cpu().numpy(), sstats.cpu().numpy()
         for r in range(rows):
             m, Z = oracle.softmax_stats(xf[r], T)
             assert st[r, 0] == m
             assert abs(st[r, 1] - Z) <= 1e-5 * Z, (r, st[r, 1], Z)
+            for k in range(S):   # every step: (its maximum, its sum against that maximum)
+                ms, Zs = oracle.softmax_stats(xf[r, k * E:(k + 1) * E], T)
+                assert sst[r, k, 0] == ms and abs(sst[r, k, 1] - Zs) <= 1e-5 * Zs, (r, k)
     assert tr.tr_get_status() == 0
 
 
@@ -112,14 +119,16 @@ def test_accept_sampled_matches_oracle(tr, dtype, T):
         U = np.stack([synth.uniforms(U_SEED + trial, 0, b, N, 9) for b in range(B)])
         ids = torch.zeros(B * N, 8, dtype=torch.int32, device="cuda")
         stats = torch.zeros(B * N, 2, dtype=torch.float32, device="cuda")
-        tr.tr_topk_softmax(xd, 8, T, ids, None, stats, tr.workspace(tr.tr_topk_workspace_bytes(B * N, V, 8)))
+        sstats = torch.zeros(B * N, tr.tr_softmax_steps(V, xd.dtype), 2, dtype=torch.float32, device="cuda")
+        tr.tr_topk_softmax(xd, 8, T, ids, None, stats, sstats,
+                           tr.workspace(tr.tr_topk_workspace_bytes(B * N, V, 8)))
         tokd = torch.from_numpy(tok.astype(np.int32)).cuda()
         acc = torch.zeros(B, dtype=torch.int32, device="cuda")
         path = torch.zeros(B, plan.max_depth + 1, dtype=torch.int32, device="cuda")
         com = torch.zeros_like(path)
         bonus = torch.zeros(B, dtype=torch.int32, device="cuda")
-        tr.tr_accept_sampled(tree, tokd, ids.view(B, N, 8), xd, stats, T, torch.from_numpy(U).cuda(), acc, path,
-                             com, bonus)
+        tr.tr_accept_sampled(tree, tokd, ids.view(B, N, 8), xd, stats, sstats, T, torch.from_numpy(U).cuda(), acc,
+                             path, com, bonus)
         assert tr.tr_get_status() == 0
         for b in range(B):
             a, p, c, y, (tm, dm), cdf = oracle.accept_sampled(plan, tok[b], xf[b * N:(b + 1) * N], T, U[b])
