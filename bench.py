@@ -42,10 +42,14 @@ PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustaine
 # dram bytes per launch of the dominant kernel from an ncu capture of this
 # workload (dram__bytes_read.sum + dram__bytes_write.sum, mean of two launches),
 # valid only while the kernel's sources are unchanged (sha256 of the files)
-TRAFFIC = {"attn": {"bytes": 631460000 + 2725000, "sha": "907250de7fad5a9d", "files": ("tr_attn.cu", "tr_sm100.cuh")}}
+TRAFFIC = {"attn": {"bytes": 631503000 + 2424000, "sha": "0813abab6b001823", "files": ("tr_attn.cu", "tr_sm100.cuh")}}
 
 
 PRIME_CYCLES = 2_000_000   # about 1 ms of device time at the GB300's clocks
+
+# ex2.approx.f32 results per SM per clock on this GPU, measured with a loop of
+# independent exponentials at 4, 8 and 16 warps per SM (31.7 - 32.8)
+EXP2_PER_SM_CLK = 32
 
 
 def load_peaks():
@@ -682,16 +686,17 @@ def main():
         traffic = tr_["bytes"] if tr_ and tr_["sha"] == src_sha(*tr_["files"]) and args.workload == "batched" else None
         flops, exps = (float(np.mean(x)) for x in zip(*res["attn_work"]))
         tf = flops / (a_ms * 1e-3) / 1e12
-        # exp2 units: 16 per SM per clock (nominal), at the sampled SM clock
+        # exp2: 32 per SM per clock, measured on this GPU with a loop of
+        # independent ex2.approx.ftz.f32 (31.7-32.8 at 4-16 warps per SM)
         sm_mhz = res["clocks"].get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
-        exp_peak = 16 * res["sm_count"] * sm_mhz * 1e6 / 1e9
+        exp_peak = EXP2_PER_SM_CLK * res["sm_count"] * sm_mhz * 1e6 / 1e9
         exp_rate = exps / (a_ms * 1e-3) / 1e9
         hbm = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak}
         tensor = {"bound": "tensor", "achieved": tf, "peak": float(peaks["bf16_tflops"]), "unit": "TFLOP/s",
                   "frac": tf / float(peaks["bf16_tflops"]), "flops_per_launch": flops}
         exp = {"achieved": exp_rate, "peak": exp_peak, "unit": "Gexp2/s", "frac": exp_rate / exp_peak,
-               "peak_source": "16 exp2 per SM per clock x %d SMs x %.0f MHz (nominal unit count)"
-                              % (res["sm_count"], sm_mhz)}
+               "peak_source": "%d exp2 per SM per clock (measured) x %d SMs x %.0f MHz"
+                              % (EXP2_PER_SM_CLK, res["sm_count"], sm_mhz)}
         # grouped-query heads read each K/V tile for several query heads: the
         # tensor pipe, not HBM, is the bound there
         main, other = (tensor, hbm) if wl.Hq != wl.Hkv else (hbm, tensor)

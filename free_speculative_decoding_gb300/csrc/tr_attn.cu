@@ -7,10 +7,15 @@
 //
 // Work decomposition (stream-K): a "pair" is (sequence, KV head, group of MT
 // query heads); its keys are ceil(L/64) cache tiles of 64 keys followed by
-// ceil(N/64) tree tiles.  All pairs' tiles form one sequence that is cut into
-// equal contiguous ranges, one per CTA (one CTA per SM, fewer for a small
-// batch), so every SM streams the same number of K/V bytes whatever the mix
-// of prefix lengths.  A pair that lies inside one range is finished in place;
+// ceil(N/64) tree tiles.  The tiles of all (sequence, KV head) are laid end to
+// end and cut into equal contiguous ranges, one per CTA group (one CTA per
+// SM, fewer for a small batch), so every SM streams the same number of K/V
+// bytes whatever the mix of prefix lengths.  A group is GS CTAs, one per
+// query-head group of a KV head (GS = Hq / (Hkv MT) when that fits the grid,
+// else 1 and those heads are laid end to end as well): the CTAs of a group
+// walk the same key tiles at the same pace, each for its own query heads, so
+// a K/V tile that one of them brings into L2 is read from there by the
+// others.  A pair that lies inside one range is finished in place;
 // a pair cut by range boundaries leaves an (m, l, O) partial per part (two
 // slots per CTA), and the part that finishes last merges them.  In stream-K
 // order that is usually a CTA's last segment, whose partner part finished long
@@ -37,9 +42,11 @@
 //               (key < L for the cache, ancestor bit for the tree), exp2 with a
 //               running maximum that only rescales O when it grows by more
 //               than 2^8, and P written back over the S columns it came from.
-//               P goes in two bf16 parts, hi = bf16(p) and lo = bf16(p - hi),
-//               both multiplied with V, so the weights reach the accumulator
-//               with ~2^-17 relative error instead of bf16's 2^-9.  At the end
+//               P goes in two bf16 parts, hi = p truncated to bf16 and
+//               lo = bf16(p - hi), both multiplied with V, so the weights reach
+//               the accumulator with at most 2^-15 relative error instead of
+//               bf16's 2^-9 (the truncation packs hi with one byte permute
+//               instead of a conversion).  At the end
 //               of a segment the same threads normalise O or write the
 //               partial.
 // TMEM holds two O accumulators (128 columns each) and four S/P buffers of
@@ -120,6 +127,8 @@ struct AttnArgs {
   int *cnt;           // [pairs] parts finished, back to zero after the merge
   unsigned *status;
   int B, N, Hq, Hkv, G, HG, cap;
+  int GS;   // CTAs per group: one per query-head group of a KV head (HG), or 1
+  int HPS;  // query-head groups laid end to end per KV head in the tile order: HG / GS
   int q_rows, c_rows, t_rows;  // TMA box heights (at most the tensor's extent)
   float scale_log2;
   unsigned long long wait_ns;  // limit of every bounded wait
@@ -127,8 +136,13 @@ struct AttnArgs {
 
 __device__ __forceinline__ int tiles_per_pair(int Lb, int N) { return (Lb + BN - 1) / BN + (N + BN - 1) / BN; }
 
-// Range of global tiles owned by CTA c of `grid`.
-__device__ __forceinline__ long long range_start(long long total, int c, int grid) { return total * c / grid; }
+// Range of global tiles owned by CTA group c of `groups`.
+__device__ __forceinline__ long long range_start(long long total, int c, int groups) { return total * c / groups; }
+
+// Group whose range holds global tile t (the inverse of range_start).
+__device__ __forceinline__ int range_owner(long long t, long long total, int groups) {
+  return (int)(((t + 1) * groups + total - 1) / total - 1);
+}
 
 // A run of consecutive tiles of one pair inside one CTA's range.
 struct Seg {
@@ -153,8 +167,8 @@ __device__ __forceinline__ Seg decode(long long t, long long t_lo, long long t_h
   const long long r = t - pref[lo];
   const int pib = (int)(r / tpp);
   s.j0 = (int)(r % tpp);
-  s.g = pib / a.HG;
-  s.hg = pib % a.HG;
+  s.g = pib / a.HPS;
+  s.hg = (pib % a.HPS) * a.GS + (int)(blockIdx.x % a.GS);  // query-head group within the KV head
   s.pair = (s.b * a.Hkv + s.g) * a.HG + s.hg;
   s.n = (int)min((long long)(tpp - s.j0), t_hi - t);
   s.n_ct = (s.Lb + BN - 1) / BN;
@@ -254,15 +268,16 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     int acc = 0;
     for (int b = 0; b < a.B; ++b) {
       bars->pref[b] = acc;
-      acc += tiles_per_pair(bars->Ls[b], N) * a.Hkv * a.HG;
+      acc += tiles_per_pair(bars->Ls[b], N) * a.Hkv * a.HPS;
     }
     bars->pref[a.B] = acc;
   }
   __syncthreads();
   const uint32_t tmem = bars->tmem;
   const long long total = bars->pref[a.B];
-  const long long t_lo = range_start(total, blockIdx.x, gridDim.x);
-  const long long t_hi = range_start(total, blockIdx.x + 1, gridDim.x);
+  const int groups = (int)gridDim.x / a.GS, grp_id = (int)blockIdx.x / a.GS;
+  const long long t_lo = range_start(total, grp_id, groups);
+  const long long t_hi = range_start(total, grp_id + 1, groups);
 
   auto give_up = [&]() {
     if (!*abort) {
@@ -480,8 +495,10 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     int gt = 0, sc = 0, n_split = 0;
     bool ok = true;
+    const int cg = (int)blockIdx.x % a.GS;  // this CTA's place in its group
     for (long long t = t_lo; t < t_hi && ok; ++sc) {
       const Seg sg = decode(t, t_lo, t_hi, bars->pref, bars->Ls, a);
+      const long long p_first = t - sg.j0;  // the pair's first tile in the global order
       t += sg.n;
       const int T = sg.n;
       const int h = sg.g * a.G + sg.hg * MT + mt;
@@ -523,7 +540,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           }
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent chains
 #pragma unroll
-          for (int c = 0; c < BN; ++c) mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+          for (int c = 0; c < BN; c += 2) mx4[(c >> 1) & 3] = fmax3(mx4[(c >> 1) & 3], sv[c], sv[c + 1]);
           // the scale is positive, so the maximum of the raw scores scales to the scaled maximum
           const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
           const float m_new = fmaxf(m_run, mx);
@@ -564,9 +581,12 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
               const float p0 = ex2(fmaf(sv[c], a.scale_log2, -m_sub));
               const float p1 = ex2(fmaf(sv[c + 1], a.scale_log2, -m_sub));
               l4[q & 3] += p0 + p1;
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __low2float(hi), p1 - __high2float(hi));
-              whi[q] = *reinterpret_cast<const uint32_t *>(&hi);
+              // hi: p truncated to bf16 (its upper 16 bits, packed by one byte
+              // permute); lo: the exact remainder rounded to bf16
+              const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - __uint_as_float(u0 & 0xffff0000u),
+                                                              p1 - __uint_as_float(u1 & 0xffff0000u));
+              whi[q] = __byte_perm(u0, u1, 0x7632);
               wlo[q] = *reinterpret_cast<const uint32_t *>(&lo);
             }
             tmem_st16_nowait(scol + half * 16, whi);
@@ -585,14 +605,17 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         m_run = -INFINITY;
         l_run = 0.f;
       }
-      // the CTAs that own parts of a split pair: CTA c owns
-      // [total*c/grid, total*(c+1)/grid), so the owner of tile t is ceil((t+1)*grid/total) - 1
+      // the CTA groups that own parts of a split pair: group q owns
+      // [total*q/groups, total*(q+1)/groups); its CTA for these query heads is q*GS + cg
       const long long p_total = bars->pref[a.B];
-      const int p_grid = (int)gridDim.x;
-      const long long p_first = bars->pref[sg.b] + (long long)(sg.g * a.HG + sg.hg) * tiles_per_pair(sg.Lb, N);
       const long long p_last = p_first + tiles_per_pair(sg.Lb, N) - 1;
-      const int pc0 = (int)(((p_first + 1) * p_grid + p_total - 1) / p_total - 1);
-      const int pc1 = (int)(((p_last + 1) * p_grid + p_total - 1) / p_total - 1);
+      const int pc0 = range_owner(p_first, p_total, groups), pc1 = range_owner(p_last, p_total, groups);
+      // with fewer tiles than groups some ranges are empty, and such a group
+      // between the owners holds no part of the pair
+      auto owns = [&](int q) { return range_start(p_total, q, groups) < range_start(p_total, q + 1, groups); };
+      int others = 0;  // parts of this pair in other CTAs
+      if (!sg.complete)
+        for (int q = pc0; q <= pc1; ++q) others += q != grp_id && owns(q) ? 1 : 0;
       float2 other = make_float2(-INFINITY, 0.f);
       if (MT == 1) {
         // A split pair whose other parts have all left their partials (at most
@@ -601,7 +624,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         if (threadIdx.x == 128 && !sg.complete) {
           int seen;
           asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(a.cnt + sg.pair) : "memory");
-          bars->mrg_early = pc1 - pc0 <= kEarlyParts && seen == pc1 - pc0;
+          bars->mrg_early = others <= kEarlyParts && seen == others;
         }
         // both warpgroups publish their (m, l); each then finishes half of the d columns
         bars->ml_x[sc & 1][grp][r] = make_float2(m_run, l_run);
@@ -620,45 +643,55 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       constexpr int COLS = MT == 1 ? kD / 2 : kD;  // columns this unit finishes
       const int col0 = MT == 1 ? grp * COLS : 0;
       const bool early = MT == 1 && !sg.complete && bars->mrg_early;
-      const int slot_pc0 = pc0 * 2 + (range_start(p_total, pc0, p_grid) < p_first ? 1 : 0);
-      auto part_row = [&](int c) {
-        const int slot = c == pc0 ? slot_pc0 : c * 2;
+      const int slot_pc0 = (pc0 * a.GS + cg) * 2 + (range_start(p_total, pc0, groups) < p_first ? 1 : 0);
+      auto part_row = [&](int q) {
+        const int slot = q == pc0 ? slot_pc0 : (q * a.GS + cg) * 2;
         return ((long long)slot * MT + mt) * N + r;
       };
       if (early) {
         if (warp_active) {
-          __threadfence();
-          // the other parts' (m, l) and rows, this part's (M, l) from above
-          float wk[kEarlyParts];
-          long long rk[kEarlyParts];
+          // No fence is needed before reading the other parts: each part
+          // fenced its writes before counting itself, the counter was read
+          // with acquire semantics, and that thread's mbarrier arrival
+          // (release) and this thread's wait (acquire) order these loads after it.
+          // The first other part's row (this warpgroup's columns) and every
+          // other part's (m, l) are requested before any is used: the loads
+          // queue behind the other CTAs' K/V streams, so each round trip
+          // costs microseconds.
+          int rk[kEarlyParts];  // partial rows: below 2 * grid * N
           int nk = 0;
-          float Mx = M;
 #pragma unroll 1
-          for (int c = pc0; c <= pc1; ++c) {
-            if (c == (int)blockIdx.x) continue;
-            rk[nk] = part_row(c);
-            const float2 ml = row_valid ? __ldcg(&a.part_ml[rk[nk]]) : make_float2(-INFINITY, 0.f);
-            wk[nk] = ml.x;  // the maximum for now, the weight below
-            Mx = fmaxf(Mx, ml.x);
-            ++nk;
-          }
+          for (int q = pc0; q <= pc1 && nk < kEarlyParts; ++q)
+            if (q != grp_id && owns(q)) rk[nk++] = (int)part_row(q);
+          float4 o1[COLS / 4];
+          const float4 *src1 = reinterpret_cast<const float4 *>(a.part_o + (long long)rk[0] * kD + col0);
+#pragma unroll
+          for (int i = 0; i < COLS / 4; ++i) o1[i] = nk > 0 && row_valid ? __ldcg(src1 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          float2 mlk[kEarlyParts];
+#pragma unroll
+          for (int k = 0; k < kEarlyParts; ++k)
+            mlk[k] = k < nk && row_valid ? __ldcg(&a.part_ml[rk[k]]) : make_float2(-INFINITY, 0.f);
+          float Mx = M;  // this part's maximum from above
+#pragma unroll
+          for (int k = 0; k < kEarlyParts; ++k) Mx = fmaxf(Mx, mlk[k].x);
           const float wown = M == -INFINITY ? 0.f : ex2(M - Mx);
           float den = l * wown;
-#pragma unroll 1
-          for (int k = 0; k < nk; ++k) {
-            const float w = wk[k] == -INFINITY ? 0.f : ex2(wk[k] - Mx);
-            den += (row_valid ? __ldcg(&a.part_ml[rk[k]]).y : 0.f) * w;
-            wk[k] = w;
+          float wk[kEarlyParts];
+#pragma unroll
+          for (int k = 0; k < kEarlyParts; ++k) {
+            wk[k] = mlk[k].x == -INFINITY ? 0.f : ex2(mlk[k].x - Mx);
+            den += mlk[k].y * wk[k];
           }
           const float inv = den > 0.f ? 1.f / den : 0.f;  // > 0 for a valid row: every node sees itself
           const float w0 = (grp == 0 ? wa : wb) * wown, w1 = (grp == 0 ? wb : wa) * wown;
           float *dst = a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD;
-#pragma unroll 1
-          for (int c0 = col0; c0 < col0 + COLS; c0 += 32) {
+#pragma unroll
+          for (int ch = 0; ch < COLS / 32; ++ch) {
+            const int c0 = col0 + ch * 32;
             float oa[32], ob[32];
             tmem_ld32(tmem + lane_off + C::o_col(0) + c0, oa);
             tmem_ld32(tmem + lane_off + C::o_col(1) + c0, ob);
-            if (c0 + 32 == col0 + COLS) {
+            if (ch == COLS / 32 - 1) {
               // the last read of the accumulators: the next segment's PV may overwrite them
               tc_fence_before();
               mbar_arrive(&bars->o_empty);
@@ -666,9 +699,17 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
             if (row_valid) {
 #pragma unroll
               for (int c = 0; c < 32; ++c) oa[c] = (w0 != 0.f ? oa[c] * w0 : 0.f) + (w1 != 0.f ? ob[c] * w1 : 0.f);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 v = o1[ch * 8 + i];
+                oa[4 * i] += v.x * wk[0];
+                oa[4 * i + 1] += v.y * wk[0];
+                oa[4 * i + 2] += v.z * wk[0];
+                oa[4 * i + 3] += v.w * wk[0];
+              }
 #pragma unroll 1
-              for (int k = 0; k < nk; ++k) {
-                const float4 *src = reinterpret_cast<const float4 *>(a.part_o + rk[k] * kD + c0);
+              for (int k = 1; k < nk; ++k) {
+                const float4 *src = reinterpret_cast<const float4 *>(a.part_o + (long long)rk[k] * kD + c0);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   const float4 v = __ldcg(src + i);
@@ -728,15 +769,13 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         // A pair shared by several CTAs (cut by range boundaries): each part
         // leaves its partial in a slot and counts itself; the last part to
         // finish merges them all and resets the counter.
-        const long long total = p_total, first = p_first;
-        const int grid = p_grid, c0 = pc0, c1 = pc1;
         __threadfence();
         mbar_arrive(&bars->mrg_in);
         if (threadIdx.x == 128) {
           int is_last = 0;
           if (mbar_wait(&bars->mrg_in, n_split & 1, abort, a.wait_ns)) {
             __threadfence();
-            is_last = atomicAdd(&a.cnt[sg.pair], 1) == c1 - c0;
+            is_last = atomicAdd(&a.cnt[sg.pair], 1) == others;
             __threadfence();
           } else {
             give_up();
@@ -748,24 +787,21 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         ++n_split;
         if (bars->mrg_last) {
           __threadfence();
-          const int slot_c0 = c0 * 2 + (range_start(total, c0, grid) < first ? 1 : 0);
           if (warp_active && row_valid) {
 #pragma unroll 1
             for (int ch = col0; ch < col0 + COLS; ch += 64) {
               float Mx = -INFINITY;
 #pragma unroll 1
-              for (int c = c0; c <= c1; ++c) {
-                const int slot = c == c0 ? slot_c0 : c * 2;
-                Mx = fmaxf(Mx, a.part_ml[((long long)slot * MT + mt) * N + r].x);
-              }
+              for (int q = pc0; q <= pc1; ++q)
+                if (owns(q)) Mx = fmaxf(Mx, a.part_ml[part_row(q)].x);
               float acc[64];
 #pragma unroll
               for (int i = 0; i < 64; ++i) acc[i] = 0.f;
               float den = 0.f;
 #pragma unroll 1
-              for (int c = c0; c <= c1; ++c) {
-                const int slot = c == c0 ? slot_c0 : c * 2;
-                const long long row = ((long long)slot * MT + mt) * N + r;
+              for (int q = pc0; q <= pc1; ++q) {
+                if (!owns(q)) continue;
+                const long long row = part_row(q);
                 const float2 ml = a.part_ml[row];
                 const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - Mx);
                 den += ml.y * w;
@@ -806,19 +842,20 @@ size_t smem_bytes() {
 }
 
 struct Plan {
-  int G, MT, HG, pairs, grid;  // grid: CTAs the workspace is laid out for (one per SM)
+  int G, MT, HG, GS, HPS, pairs, grid;  // grid: CTAs the workspace is laid out for (one per SM)
   size_t o_off, ml_off, cnt_off, total;
 };
 
 // CTAs to launch: one per SM, but never so many that a CTA gets fewer than
 // kMinTiles tiles of the largest possible work (cap keys per sequence): a
 // small batch would otherwise cut every pair into many parts, each paying the
-// start-up and the partial merge.
+// start-up and the partial merge.  Always whole groups.
 constexpr long long kMinTiles = 16;
 int launch_grid(const Plan &p, int B, int Hkv, int cap, int N) {
   const long long most = (long long)B * Hkv * p.HG * ((cap + BN - 1) / BN + (N + BN - 1) / BN);
   const long long want = (most + kMinTiles - 1) / kMinTiles;
-  return (int)std::max<long long>(1, std::min<long long>(p.grid, want));
+  const long long g = std::max<long long>(1, std::min<long long>(p.grid, want) / p.GS);
+  return (int)(g * p.GS);
 }
 
 Plan make_plan(int B, int Hq, int Hkv, int N) {
@@ -832,6 +869,10 @@ Plan make_plan(int B, int Hq, int Hkv, int N) {
   p.HG = p.G / p.MT;
   p.pairs = B * Hkv * p.HG;
   p.grid = tr_sm_count();
+  // one CTA per query-head group of a KV head in each CTA group, when that
+  // fits the grid; else those heads are laid end to end in the tile order
+  p.GS = p.HG <= p.grid ? p.HG : 1;
+  p.HPS = p.HG / p.GS;
   const size_t rows = (size_t)p.grid * 2 * p.MT * N;
   p.o_off = 0;
   p.ml_off = tr_align_up(rows * kD * sizeof(float), 256);
@@ -897,6 +938,8 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
   a.Hkv = Hkv;
   a.G = p.G;
   a.HG = p.HG;
+  a.GS = p.GS;
+  a.HPS = p.HPS;
   a.cap = cap;
   a.q_rows = (int)q_rows;
   a.c_rows = (int)c_rows;

@@ -382,6 +382,10 @@ def test_bad_token_and_full_cache_are_flagged(tr):
     ([1, 1, 0], 3, 8, 1, [5, 64, 0], None),
     ([0], 2, 4, 4, [0, 70], None),              # the root alone
     ([2, 0, 0], 1, 2, 1, [33], 40),             # a cache tensor of 40 rows
+    # far fewer tiles than the grid sized for the capacity: CTAs (groups) with
+    # empty ranges lie between the parts of a split pair
+    ("T80", 1, 1, 1, [0], 4096),
+    ("T80", 1, 4, 1, [3], 4096),
 ])
 def test_attention_matches_oracle(tr, tree_name, B, Hq, Hkv, lens, cap):
     counts = synth.TREES[tree_name] if isinstance(tree_name, str) else tree_name
