@@ -386,6 +386,11 @@ def test_bad_token_and_full_cache_are_flagged(tr):
     # empty ranges lie between the parts of a split pair
     ("T80", 1, 1, 1, [0], 4096),
     ("T80", 1, 4, 1, [3], 4096),
+    # query-head groups: one group of 64 CTAs sharing one short range (the
+    # grid rounded up to whole groups), and more query heads per KV head than
+    # SMs (one CTA per group, the heads laid end to end)
+    ("T80", 1, 64, 1, [100], None),
+    ("T80", 1, 160, 1, [700], None),
 ])
 def test_attention_matches_oracle(tr, tree_name, B, Hq, Hkv, lens, cap):
     counts = synth.TREES[tree_name] if isinstance(tree_name, str) else tree_name
