@@ -5,15 +5,15 @@
 // root-to-i path (blog "token-recycling", 完整工作流程 step 3; the
 // speculative-decoding lesson's tree attention).
 //
-// Work decomposition (stream-K): a "pair" is (sequence, KV head, group of MT
-// query heads); its keys are ceil(L/64) cache tiles of 64 keys followed by
+// Work decomposition (stream-K): a "pair" is (sequence, KV head, query
+// head); its keys are ceil(L/64) cache tiles of 64 keys followed by
 // ceil(N/64) tree tiles.  The tiles of all (sequence, KV head) are laid end to
 // end and cut into equal contiguous ranges, one per CTA group (one CTA per
 // SM, fewer for a small batch), so every SM streams the same number of K/V
 // bytes whatever the mix of prefix lengths.  A group is GS CTAs, one per
-// query-head group of a KV head (GS = Hq / (Hkv MT) when that fits the grid,
-// else 1 and those heads are laid end to end as well): the CTAs of a group
-// walk the same key tiles at the same pace, each for its own query heads, so
+// query head of a KV head (GS = Hq / Hkv when that fits the grid, else 1 and
+// those heads are laid end to end as well): the CTAs of a group walk the
+// same key tiles at the same pace, each for its own query head, so
 // a K/V tile that one of them brings into L2 is read from there by the
 // others.  A pair that lies inside one range is finished in place;
 // a pair cut by range boundaries leaves an (m, l, O) partial per part (two
@@ -53,11 +53,10 @@
 // 64 columns; a buffer is reused by the QK product four tiles later, once the
 // PV product that read its P has completed.  The two softmax warpgroups take
 // alternate tiles into their own accumulators (combined at the end of a
-// segment).  The kernel is written for MT query heads per pair; it launches
-// with MT = 1 (grouped-query heads too, one pair per query head), since two
-// heads per K/V tile (MT = 2: one warpgroup and one accumulator per head, 256
-// query rows per tile, half the K/V reads) measured slower on grouped-query
-// shapes, which are bound by the tensor pipe and the exponentials.
+// segment).  Grouped-query heads also get one pair per query head: two heads
+// per K/V tile (one warpgroup and one accumulator per head, 256 query rows
+// per tile, half the K/V reads) measured slower on grouped-query shapes,
+// which are bound by the tensor pipe and the exponentials.
 //
 // Every wait is bounded in time; a wait that gives up sets TR_DEV_TIMEOUT and
 // raises a block-wide abort flag; the roles drain their in-flight copies and
@@ -74,7 +73,6 @@ constexpr float kRescaleLog2 = 8.f; // O is rescaled only when the row maximum g
 constexpr int kMaxB = 1024;
 constexpr int kEarlyParts = 4;      // other parts a split pair may have for the direct merge
 
-template <int MT>
 struct Cfg {
   // One Q buffer (the next segment's Q is prefetched into L2) leaves room for
   // five K and five V stages: a tile's copy lands ~1.25 us after it is issued,
@@ -82,39 +80,37 @@ struct Cfg {
   // so each ring must hold more than that latency's worth of tiles.  Measured
   // on one box against two Q buffers with 3 K + 5 V stages: 0.1294 -> 0.1229 ms
   // (batched workload), 0.1134 -> 0.1098 ms (grouped-query workload).
-  static constexpr int QB = 1;                    // Q buffers
-  static constexpr int KS = MT == 1 ? 5 : 4;      // K ring stages
+  static constexpr int KS = 5;                    // K ring stages
   static constexpr int VS = 5;                    // V ring stages
-  static constexpr int GROUPS = MT == 1 ? 2 : 1;  // softmax warpgroups sharing one query head
-  static constexpr int NSB = 4 / MT;              // S/P buffers in TMEM
+  static constexpr int GROUPS = 2;                // softmax warpgroups taking alternate tiles
+  static constexpr int NSB = 4;                   // S/P buffers in TMEM
   static constexpr int Q_HALF = 128 * 128;        // 128 rows x 64 bf16 (one d-half), bytes
   static constexpr int KV_HALF = 64 * 128;        // 64 keys x 64 bf16
   static constexpr int KV_TILE = 2 * KV_HALF;
   static constexpr int OFF_Q = 0;
-  static constexpr int Q_BUF = MT * 2 * Q_HALF;
-  static constexpr int OFF_K = OFF_Q + QB * Q_BUF;
+  static constexpr int Q_BUF = 2 * Q_HALF;
+  static constexpr int OFF_K = OFF_Q + Q_BUF;
   static constexpr int OFF_V = OFF_K + KS * KV_TILE;
   static constexpr int OFF_BAR = OFF_V + VS * KV_TILE;
   static constexpr int SOFT = 256;                // softmax threads: two warpgroups
   static constexpr int THREADS = 128 + SOFT;
   static constexpr uint32_t TMEM_COLS = 512;
   __host__ __device__ static constexpr uint32_t o_col(int o) { return (uint32_t)(o * kD); }
-  __host__ __device__ static constexpr uint32_t s_col(int buf, int m) { return (uint32_t)(2 * kD + (buf * MT + m) * BN); }
+  __host__ __device__ static constexpr uint32_t s_col(int buf) { return (uint32_t)(2 * kD + buf * BN); }
 };
-static_assert(Cfg<1>::s_col(Cfg<1>::NSB - 1, 0) + BN <= Cfg<1>::TMEM_COLS, "TMEM budget");
+static_assert(Cfg::s_col(Cfg::NSB - 1) + BN <= Cfg::TMEM_COLS, "TMEM budget");
 
-template <int MT>
 struct Bars {
-  static constexpr int QB = Cfg<MT>::QB, KS = Cfg<MT>::KS, VS = Cfg<MT>::VS, NSB = Cfg<MT>::NSB;
-  uint64_t q_full[QB], q_empty[QB];
+  static constexpr int KS = Cfg::KS, VS = Cfg::VS, NSB = Cfg::NSB;
+  uint64_t q_full, q_empty;
   uint64_t k_full[KS], k_empty[KS], v_full[VS], v_empty[VS];
   uint64_t s_full[NSB], p_full[NSB], pv_done[NSB];
   uint64_t o_full, o_empty, drain, ml_ready;
   uint64_t mrg_in, mrg_go;  // hand-off of a pair shared by several CTAs
   uint32_t tmem;
   int abort, mrg_last;
-  int mrg_early;  // MT == 1: every other part of this split pair has already left its partial
-  float2 ml_x[2][2][128];  // each warpgroup's (m, l) per row, by segment parity (MT == 1)
+  int mrg_early;  // every other part of this split pair has already left its partial
+  float2 ml_x[2][2][128];  // each warpgroup's (m, l) per row, by segment parity
   int Ls[kMaxB];
   int pref[kMaxB + 1];  // first tile of sequence b in the global tile order
 };
@@ -122,13 +118,13 @@ struct Bars {
 struct AttnArgs {
   const int32_t *L;
   float *O;
-  float *part_o;      // [grid, 2, MT, N, d]
-  float2 *part_ml;    // [grid, 2, MT, N]
+  float *part_o;      // [grid, 2, N, d]
+  float2 *part_ml;    // [grid, 2, N]
   int *cnt;           // [pairs] parts finished, back to zero after the merge
   unsigned *status;
-  int B, N, Hq, Hkv, G, HG, cap;
-  int GS;   // CTAs per group: one per query-head group of a KV head (HG), or 1
-  int HPS;  // query-head groups laid end to end per KV head in the tile order: HG / GS
+  int B, N, Hq, Hkv, G, cap;  // G = Hq / Hkv query heads per KV head
+  int GS;   // CTAs per group: one per query head of a KV head (G), or 1
+  int HPS;  // query heads laid end to end per KV head in the tile order: G / GS
   int q_rows, c_rows, t_rows;  // TMA box heights (at most the tensor's extent)
   float scale_log2;
   unsigned long long wait_ns;  // limit of every bounded wait
@@ -168,8 +164,8 @@ __device__ __forceinline__ Seg decode(long long t, long long t_lo, long long t_h
   const int pib = (int)(r / tpp);
   s.j0 = (int)(r % tpp);
   s.g = pib / a.HPS;
-  s.hg = (pib % a.HPS) * a.GS + (int)(blockIdx.x % a.GS);  // query-head group within the KV head
-  s.pair = (s.b * a.Hkv + s.g) * a.HG + s.hg;
+  s.hg = (pib % a.HPS) * a.GS + (int)(blockIdx.x % a.GS);  // query head within the KV head
+  s.pair = (s.b * a.Hkv + s.g) * a.G + s.hg;
   s.n = (int)min((long long)(tpp - s.j0), t_hi - t);
   s.n_ct = (s.Lb + BN - 1) / BN;
   s.complete = s.j0 == 0 && s.n == tpp;
@@ -201,26 +197,23 @@ struct Cursor {
   }
 };
 
-template <int MT>
-__global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKc,
                    const __grid_constant__ CUtensorMap tmVc, const __grid_constant__ CUtensorMap tmKt,
                    const __grid_constant__ CUtensorMap tmVt, const AttnArgs a, const __grid_constant__ TreeDev tree) {
   using namespace sm100;
-  using C = Cfg<MT>;
+  using C = Cfg;
   constexpr int KS = C::KS, VS = C::VS, NSB = C::NSB, GROUPS = C::GROUPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  Bars<MT> *bars = (Bars<MT> *)(smem + C::OFF_BAR);
+  Bars *bars = (Bars *)(smem + C::OFF_BAR);
   volatile int *abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
 
   if (threadIdx.x == 0) {
-    for (int q = 0; q < C::QB; ++q) {
-      mbar_init(&bars->q_full[q], 1);
-      mbar_init(&bars->q_empty[q], 1);
-    }
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < KS; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -231,7 +224,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     }
     for (int b = 0; b < NSB; ++b) {
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 128 * MT);
+      mbar_init(&bars->p_full[b], 128);
       mbar_init(&bars->pv_done[b], 1);
     }
     mbar_init(&bars->o_full, 1);
@@ -354,53 +347,42 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     // S = Q.K^T of tile i once its Q and K have landed and the S/P buffer's
     // previous PV product has completed.  The whole warp runs the loop, so its
     // control flow and operands stay warp-uniform; one elected lane issues.
-    // This warp also loads Q: with two buffers the next segment's Q is loaded
-    // while the current one runs; with one, the next Q is prefetched into L2.
-    constexpr int QB = C::QB;
+    // This warp also loads Q into the one buffer, once the previous segment's
+    // last product is done; the next segment's Q is prefetched into L2 meanwhile.
     constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
     const uint64_t dq0 = desc_kmajor_sw128(smem_u32(smem + C::OFF_Q));
     const uint64_t dk0 = desc_kmajor_sw128(smem_u32(smem + C::OFF_K));
-    int q_armed[QB];  // parity of the last Q load into each buffer, -1 for none
-    for (int q = 0; q < QB; ++q) q_armed[q] = -1;
+    int q_armed = -1;  // parity of the last Q load, -1 for none
     auto load_q = [&](const Seg &sg, int sc_of) {
-      const int buf = sc_of % QB;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&bars->q_full[buf], (uint32_t)(MT * 2 * a.q_rows * 128));
-        for (int m = 0; m < MT; ++m) {
-          const int h = sg.g * a.G + sg.hg * MT + m;
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(smem + C::OFF_Q + buf * C::Q_BUF + (m * 2 + half) * C::Q_HALF, &tmQ, &bars->q_full[buf],
-                        half * 64, h, sg.b * N);
-        }
+        mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(2 * a.q_rows * 128));
+        const int h = sg.g * a.G + sg.hg;
+        for (int half = 0; half < 2; ++half)
+          tma_load_3d(smem + C::OFF_Q + half * C::Q_HALF, &tmQ, &bars->q_full, half * 64, h, sg.b * N);
       }
       __syncwarp();
-      q_armed[buf] = (sc_of / QB) & 1;
+      q_armed = sc_of & 1;
     };
     Cursor cq;
     cq.init(t_lo, t_hi, bars->pref, bars->Ls, a);
     const int n_all = (int)(t_hi - t_lo);
     if (lane == 0) tma_prefetch_desc(&tmQ);
-    if (n_all > 0) {
-      load_q(cq.sg, 0);
-      if (QB == 2 && cq.t + cq.sg.n < t_hi) load_q(decode(cq.t + cq.sg.n, t_lo, t_hi, bars->pref, bars->Ls, a), 1);
-    }
+    if (n_all > 0) load_q(cq.sg, 0);
     for (int i = 0; i < n_all; ++i) {
       const int sb = i % NSB, ks = i % KS;
-      const int qb = cq.sc % QB;
       if (cq.u == 0) {
         const long long t_next = cq.t + cq.sg.n;  // first tile of the next segment
-        if (QB == 1 && cq.sc > 0) {
-          // the only buffer held the previous segment's Q: refill it once its last product is done
-          if (!wwait(&bars->q_empty[0], (cq.sc - 1) & 1)) break;
+        if (cq.sc > 0) {
+          // the buffer held the previous segment's Q: refill it once its last product is done
+          if (!wwait(&bars->q_empty, (cq.sc - 1) & 1)) break;
           load_q(cq.sg, cq.sc);
         }
-        if (QB == 1 && t_next < t_hi && lane == 0) {
+        if (t_next < t_hi && lane == 0) {
           const Seg nx = decode(t_next, t_lo, t_hi, bars->pref, bars->Ls, a);
-          for (int m = 0; m < MT; ++m)
-            for (int half = 0; half < 2; ++half)
-              tma_prefetch_l2_3d(&tmQ, half * 64, nx.g * a.G + nx.hg * MT + m, nx.b * N);
+          for (int half = 0; half < 2; ++half)
+            tma_prefetch_l2_3d(&tmQ, half * 64, nx.g * a.G + nx.hg, nx.b * N);
         }
-        if (!wwait(&bars->q_full[qb], (cq.sc / QB) & 1)) break;
+        if (!wwait(&bars->q_full, cq.sc & 1)) break;
       }
       if (!wwait(&bars->k_full[ks], (i / KS) & 1)) break;
       if (i >= NSB && !wwait(&bars->pv_done[sb], ((i / NSB) - 1) & 1)) break;
@@ -409,33 +391,19 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         // descriptor start addresses count 16-byte units
         const uint64_t dk = dk0 + (uint64_t)(ks * (C::KV_TILE >> 4));
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const uint64_t dq = dq0 + (uint64_t)((qb * C::Q_BUF + m * 2 * C::Q_HALF) >> 4);
-#pragma unroll
-          for (int k = 0; k < kD / 16; ++k)
-            mma_bf16(tmem + C::s_col(sb, m), dq + (uint64_t)(((k >> 2) * C::Q_HALF + (k & 3) * 32) >> 4),
-                     dk + (uint64_t)(((k >> 2) * C::KV_HALF + (k & 3) * 32) >> 4), kIdesc, k > 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < kD / 16; ++k)
+          mma_bf16(tmem + C::s_col(sb), dq0 + (uint64_t)(((k >> 2) * C::Q_HALF + (k & 3) * 32) >> 4),
+                   dk + (uint64_t)(((k >> 2) * C::KV_HALF + (k & 3) * 32) >> 4), kIdesc, k > 0 ? 1u : 0u);
         mma_commit(&bars->k_empty[ks]);
         mma_commit(&bars->s_full[sb]);
-        if (cq.last()) mma_commit(&bars->q_empty[qb]);
+        if (cq.last()) mma_commit(&bars->q_empty);
       }
       __syncwarp();
-      if (QB == 2 && cq.u == 0 && cq.sc > 0) {
-        // after the segment's first product: the previous segment's buffer
-        // takes the next segment's Q once its last product is done
-        const long long t_next = cq.t + cq.sg.n;
-        if (t_next < t_hi) {
-          if (!wwait(&bars->q_empty[qb ^ 1], ((cq.sc - 1) / QB) & 1)) break;
-          load_q(decode(t_next, t_lo, t_hi, bars->pref, bars->Ls, a), cq.sc + 1);
-        }
-      }
       cq.advance(t_lo, t_hi, bars->pref, bars->Ls, a);
     }
     if (*abort) {
-      // let the Q copies already issued land before the CTA can exit
-      for (int q = 0; q < QB; ++q)
-        if (q_armed[q] >= 0) mbar_drain(&bars->q_full[q], (uint32_t)q_armed[q]);
+      // let the Q copy already issued land before the CTA can exit
+      if (q_armed >= 0) mbar_drain(&bars->q_full, (uint32_t)q_armed);
     }
     if (elect_one()) mma_commit(&bars->drain);
     __syncwarp();
@@ -459,17 +427,14 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       if (elect_one()) {
         const uint64_t dv = dv0 + (uint64_t)(vs * (C::KV_TILE >> 4));
         const uint32_t first = cp.u >= GROUPS ? 1u : 0u;
+        const uint32_t d_o = tmem + C::o_col(i & 1);  // tile i's warpgroup owns accumulator i & 1
+        const uint32_t a_p = tmem + C::s_col(sb);
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          const uint32_t d_o = tmem + C::o_col(MT == 1 ? (i & 1) : m);  // MT == 1: tile i's warpgroup owns accumulator i & 1
-          const uint32_t a_p = tmem + C::s_col(sb, m);
+        for (int part = 0; part < 2; ++part)
 #pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
-              mma_bf16_ts(d_o, a_p + part * 32 + k * 8, dv + (uint64_t)(k * (2048 >> 4)), kIdesc,
-                          (part > 0 || k > 0) ? 1u : first);
-        }
+          for (int k = 0; k < BN / 16; ++k)
+            mma_bf16_ts(d_o, a_p + part * 32 + k * 8, dv + (uint64_t)(k * (2048 >> 4)), kIdesc,
+                        (part > 0 || k > 0) ? 1u : first);
         mma_commit(&bars->v_empty[vs]);
         mma_commit(&bars->pv_done[sb]);
         if (cp.last()) mma_commit(&bars->o_full);
@@ -482,10 +447,8 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     mbar_drain(&bars->drain, 0);
   } else {
     // -------------------------------------------------------------- softmax
-    const int su = (warp - 4) >> 2;            // softmax unit: warpgroup (MT == 1) or query head (MT == 2)
-    const int grp = MT == 1 ? su : 0;
-    const int mt = MT == 1 ? 0 : su;
-    const int oacc = su;                       // this unit's O accumulator
+    const int grp = (warp - 4) >> 2;           // softmax warpgroup: takes tiles grp, grp + 2, ...
+    const int oacc = grp;                      // this warpgroup's O accumulator
     const int quad = warp & 3;                 // TMEM lanes quad*32 .. +31
     const int r = quad * 32 + lane;
     const bool warp_active = quad * 32 < N;
@@ -501,12 +464,12 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       const long long p_first = t - sg.j0;  // the pair's first tile in the global order
       t += sg.n;
       const int T = sg.n;
-      const int h = sg.g * a.G + sg.hg * MT + mt;
+      const int h = sg.g * a.G + sg.hg;
       float m_run = -INFINITY, l_run = 0.f;  // running maximum (log2 units) and sum
       int done_here = 0;  // tiles of this segment this unit has folded into its accumulator
       for (int u = 0; u < T && ok; ++u) {
         const int gtt = gt + u, sb = gtt % NSB;
-        if (MT == 1 && (gtt & 1) != grp) continue;  // the other warpgroup's tile
+        if ((gtt & 1) != grp) continue;  // the other warpgroup's tile
         // also for inactive warps: their p_full arrival must not run ahead
         // into the buffer's next use
         if (!wwait(&bars->s_full[sb], (gtt / NSB) & 1)) {
@@ -515,7 +478,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         }
         tc_fence_after();
         if (warp_active) {
-          const uint32_t scol = tmem + lane_off + C::s_col(sb, mt);
+          const uint32_t scol = tmem + lane_off + C::s_col(sb);
           float sv[BN];
           tmem_ld64(scol, sv);
           const int j = sg.j0 + u;
@@ -616,37 +579,32 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       int others = 0;  // parts of this pair in other CTAs
       if (!sg.complete)
         for (int q = pc0; q <= pc1; ++q) others += q != grp_id && owns(q) ? 1 : 0;
-      float2 other = make_float2(-INFINITY, 0.f);
-      if (MT == 1) {
-        // A split pair whose other parts have all left their partials (at most
-        // kEarlyParts of them): this part merges straight from its accumulators
-        // instead of writing a partial, handing over and reading it back.
-        if (threadIdx.x == 128 && !sg.complete) {
-          int seen;
-          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(a.cnt + sg.pair) : "memory");
-          bars->mrg_early = others <= kEarlyParts && seen == others;
-        }
-        // both warpgroups publish their (m, l); each then finishes half of the d columns
-        bars->ml_x[sc & 1][grp][r] = make_float2(m_run, l_run);
-        mbar_arrive(&bars->ml_ready);
+      // A split pair whose other parts have all left their partials (at most
+      // kEarlyParts of them): this part merges straight from its accumulators
+      // instead of writing a partial, handing over and reading it back.
+      if (threadIdx.x == 128 && !sg.complete) {
+        int seen;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(a.cnt + sg.pair) : "memory");
+        bars->mrg_early = others <= kEarlyParts && seen == others;
       }
+      // both warpgroups publish their (m, l); each then finishes half of the d columns
+      bars->ml_x[sc & 1][grp][r] = make_float2(m_run, l_run);
+      mbar_arrive(&bars->ml_ready);
       if (!wwait(&bars->o_full, sc & 1)) break;
       tc_fence_after();
-      if (MT == 1) {
-        if (!wwait(&bars->ml_ready, sc & 1)) break;
-        other = bars->ml_x[sc & 1][grp ^ 1][r];
-      }
+      if (!wwait(&bars->ml_ready, sc & 1)) break;
+      const float2 other = bars->ml_x[sc & 1][grp ^ 1][r];
       const float M = fmaxf(m_run, other.x);
       const float wa = m_run == -INFINITY ? 0.f : ex2(m_run - M);   // this unit's accumulator
-      const float wb = other.x == -INFINITY ? 0.f : ex2(other.x - M);  // the other warpgroup's (MT == 1)
+      const float wb = other.x == -INFINITY ? 0.f : ex2(other.x - M);  // the other warpgroup's
       const float l = l_run * wa + other.y * wb;
-      constexpr int COLS = MT == 1 ? kD / 2 : kD;  // columns this unit finishes
-      const int col0 = MT == 1 ? grp * COLS : 0;
-      const bool early = MT == 1 && !sg.complete && bars->mrg_early;
+      constexpr int COLS = kD / 2;  // columns this warpgroup finishes
+      const int col0 = grp * COLS;
+      const bool early = !sg.complete && bars->mrg_early;
       const int slot_pc0 = (pc0 * a.GS + cg) * 2 + (range_start(p_total, pc0, groups) < p_first ? 1 : 0);
       auto part_row = [&](int q) {
         const int slot = q == pc0 ? slot_pc0 : (q * a.GS + cg) * 2;
-        return ((long long)slot * MT + mt) * N + r;
+        return (long long)slot * N + r;
       };
       if (early) {
         if (warp_active) {
@@ -732,17 +690,17 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         }
       } else if (warp_active) {
         const int slot = blockIdx.x * 2 + (sg.first_of_cta ? 0 : 1);
-        const long long prow_idx = ((long long)slot * MT + mt) * N + r;
+        const long long prow_idx = (long long)slot * N + r;
         const float scale_out = sg.complete ? (row_valid && l > 0.f ? 1.f / l : 0.f) : 1.f;
-        // MT == 1: fold accumulator 0 with weight w0 and accumulator 1 with w1
-        const float w0 = MT == 1 ? (grp == 0 ? wa : wb) : wa;
-        const float w1 = MT == 1 ? (grp == 0 ? wb : wa) : 0.f;
+        // fold accumulator 0 with weight w0 and accumulator 1 with w1
+        const float w0 = grp == 0 ? wa : wb;
+        const float w1 = grp == 0 ? wb : wa;
         float *dst = sg.complete ? a.O + (((long long)sg.b * N + r) * a.Hq + h) * kD : a.part_o + prow_idx * kD;
 #pragma unroll 1
         for (int c0 = col0; c0 < col0 + COLS; c0 += 32) {
           float oa[32], ob[32];
-          tmem_ld32(tmem + lane_off + C::o_col(MT == 1 ? 0 : oacc) + c0, oa);
-          if (MT == 1) tmem_ld32(tmem + lane_off + C::o_col(1) + c0, ob);
+          tmem_ld32(tmem + lane_off + C::o_col(0) + c0, oa);
+          tmem_ld32(tmem + lane_off + C::o_col(1) + c0, ob);
           if (c0 + 32 == col0 + COLS) {
             // the last read of the accumulators: the next segment's PV may overwrite them
             tc_fence_before();
@@ -752,7 +710,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
               float v = w0 != 0.f ? oa[c] * w0 : 0.f;
-              if (MT == 1 && w1 != 0.f) v += ob[c] * w1;
+              if (w1 != 0.f) v += ob[c] * w1;
               oa[c] = v * scale_out;
             }
 #pragma unroll
@@ -760,7 +718,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
               *reinterpret_cast<float4 *>(dst + c + c0) = make_float4(oa[c], oa[c + 1], oa[c + 2], oa[c + 3]);
           }
         }
-        if (!sg.complete && row_valid && (MT == 2 || grp == 0)) a.part_ml[prow_idx] = make_float2(M, l);
+        if (!sg.complete && row_valid && grp == 0) a.part_ml[prow_idx] = make_float2(M, l);
       } else {
         tc_fence_before();
         mbar_arrive(&bars->o_empty);
@@ -836,13 +794,10 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   }
 }
 
-template <int MT>
-size_t smem_bytes() {
-  return (size_t)Cfg<MT>::OFF_BAR + sizeof(Bars<MT>) + 1024;
-}
+size_t smem_bytes() { return (size_t)Cfg::OFF_BAR + sizeof(Bars) + 1024; }
 
 struct Plan {
-  int G, MT, HG, GS, HPS, pairs, grid;  // grid: CTAs the workspace is laid out for (one per SM)
+  int G, GS, HPS, pairs, grid;  // grid: CTAs the workspace is laid out for (one per SM)
   size_t o_off, ml_off, cnt_off, total;
 };
 
@@ -852,7 +807,7 @@ struct Plan {
 // start-up and the partial merge.  Always whole groups.
 constexpr long long kMinTiles = 16;
 int launch_grid(const Plan &p, int B, int Hkv, int cap, int N) {
-  const long long most = (long long)B * Hkv * p.HG * ((cap + BN - 1) / BN + (N + BN - 1) / BN);
+  const long long most = (long long)B * Hkv * p.G * ((cap + BN - 1) / BN + (N + BN - 1) / BN);
   const long long want = (most + kMinTiles - 1) / kMinTiles;
   const long long g = std::max<long long>(1, std::min<long long>(p.grid, want) / p.GS);
   return (int)(g * p.GS);
@@ -862,18 +817,16 @@ Plan make_plan(int B, int Hq, int Hkv, int N) {
   Plan p;
   p.G = Hq / Hkv;
   // one query head per pair, also for grouped-query heads: two heads per
-  // K/V tile (MT = 2) halve the K/V reads but measured slower on the
-  // grouped-query shapes tried (32 query / 8 KV heads, prefixes 4096 and
-  // 32768), which are bound by the tensor pipe and the exponentials, not HBM
-  p.MT = 1;
-  p.HG = p.G / p.MT;
-  p.pairs = B * Hkv * p.HG;
+  // K/V tile halve the K/V reads but measured slower on the grouped-query
+  // shapes tried (32 query / 8 KV heads, prefixes 4096 and 32768), which are
+  // bound by the tensor pipe and the exponentials, not HBM
+  p.pairs = B * Hkv * p.G;
   p.grid = tr_sm_count();
-  // one CTA per query-head group of a KV head in each CTA group, when that
-  // fits the grid; else those heads are laid end to end in the tile order
-  p.GS = p.HG <= p.grid ? p.HG : 1;
-  p.HPS = p.HG / p.GS;
-  const size_t rows = (size_t)p.grid * 2 * p.MT * N;
+  // one CTA per query head of a KV head in each CTA group, when that fits
+  // the grid; else those heads are laid end to end in the tile order
+  p.GS = p.G <= p.grid ? p.G : 1;
+  p.HPS = p.G / p.GS;
+  const size_t rows = (size_t)p.grid * 2 * N;
   p.o_off = 0;
   p.ml_off = tr_align_up(rows * kD * sizeof(float), 256);
   p.cnt_off = p.ml_off + tr_align_up(rows * sizeof(float2), 256);
@@ -937,7 +890,6 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.G = p.G;
-  a.HG = p.HG;
   a.GS = p.GS;
   a.HPS = p.HPS;
   a.cap = cap;
@@ -948,15 +900,14 @@ extern "C" int tr_verify_attn(const void *Q, const void *Kt, const void *Vt, con
   a.wait_ns = tr_wait_limit_ns();
   cudaStream_t s = (cudaStream_t)stream;
   const int grid = launch_grid(p, B, Hkv, cap, N);
-  static bool attr_set[1][64];
+  static bool attr_set[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[0][dev]) {
-    TR_TRY_CUDA(cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem_bytes<1>()));
-    attr_set[0][dev] = true;
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    TR_TRY_CUDA(cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes()));
+    attr_set[dev] = true;
   }
-  attn_tc_kernel<1><<<grid, Cfg<1>::THREADS, smem_bytes<1>(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
+  attn_tc_kernel<<<grid, Cfg::THREADS, smem_bytes(), s>>>(tq, tkc, tvc, tkt, tvt, a, tree->dev);
   TR_LAUNCH_CHECK();
   return TR_OK;
 }
