@@ -25,19 +25,21 @@
 //
 // Per CTA (12 warps, so each SM sub-partition hosts one helper warp and two
 // softmax warps):
-//   warp 0      TMA producer of Q (3-D map over [B*N, Hq, d]) and of the K
-//               ring: tiles of 64 keys from the cache (2-D map over
-//               [B*Hkv*cap, d]) or the tree (3-D map over [B*N, Hkv, d]);
+//   warp 0      TMA producer of the K ring: tiles of 64 keys from the cache
+//               (2-D map over [B*Hkv*cap, d]) or the tree (3-D map over
+//               [B*N, Hkv, d]);
 //   warp 2      TMA producer of the V ring, same maps for V; the two rings
 //               run independently, so a V stage still held by a PV product
 //               never stops the K stream;
-//   warp 1      loads Q (one buffer; the next segment's Q is prefetched into
-//               L2) and issues S = Q.K^T (tcgen05.mma M128 x N64 x K128, fp32 in
-//               TMEM);
+//   warp 1      loads Q (3-D map over [B*N, Hq, d]; one buffer, the next
+//               segment's Q is prefetched into L2) and issues S = Q.K^T
+//               (tcgen05.mma M128 x N64 x K128, fp32 in TMEM);
 //   warp 3      issues O += P.V (M128 x N128 x K64) with P read from TMEM and V
-//               from shared memory as an MN-major operand.  Two issuers keep
-//               each one's instruction stream short; both run warp-uniformly
-//               and issue from one elected lane;
+//               from shared memory as an MN-major operand.  One thread
+//               issues an MMA every ~68 cycles at best (measured), so the two
+//               products come from two warps, which together keep the tensor
+//               pipe busy; both run warp-uniformly and issue from one elected
+//               lane;
 //   warps 4..11 softmax, one query row per thread (one TMEM lane): the mask
 //               (key < L for the cache, ancestor bit for the tree), exp2 with a
 //               running maximum that only rescales O when it grows by more
