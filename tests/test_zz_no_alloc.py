@@ -1,10 +1,11 @@
-"""The allocation-free top-K entry point against the workspace one (GB300 only).
+"""The allocation-free top-K entry point against the oracle and the workspace one (GB300 only).
 
 tr_topk_noalloc exists for callers that cannot allocate device memory (a
 plugin whose host framework owns every buffer, a serving loop that must not
 call cudaMalloc, a foreign-function caller without an allocator).  It must
-give exactly what tr_topk gives -- top-K IDs are integers and the values are
-copied logits, so the comparison is exact, as in every top-K test here -- on
+give exactly the oracle's top-K, and so what tr_topk gives -- top-K IDs are
+integers and the values are copied logits, so the comparison is exact, as in
+every top-K test here -- on
 two calls in a row, which also shows that the shared static scratch carries no
 state from one call to the next.  This file is collected last so a
 stop-at-first-failure run has already run everything else; it also passes
@@ -15,6 +16,8 @@ import ctypes
 import numpy as np
 import pytest
 import torch
+
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +56,9 @@ def test_noalloc_matches_workspace_topk_twice(tr, rows, V, K, dtype):
     for call in range(2):
         x = (torch.round(torch.randn(rows, V, generator=g) * 8) / 8).to(dtype).cuda()   # ties included
         (ia, va), (ib, vb) = _both(tr, x, K)
+        ids_ref, vals_ref = oracle.topk_rows(x.float().cpu().numpy(), K)
+        assert np.array_equal(ib, ids_ref), "ids differ from the oracle on call %d" % call
+        assert np.array_equal(vb, vals_ref.astype(np.float32)), "values differ from the oracle on call %d" % call
         assert np.array_equal(ia, ib), "ids differ on call %d" % call
         assert np.array_equal(va, vb), "values differ on call %d" % call
         assert (ia >= 0).all()
