@@ -42,7 +42,7 @@ PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustaine
 # dram bytes per launch of the dominant kernel from an ncu capture of this
 # workload (dram__bytes_read.sum + dram__bytes_write.sum, mean of three launches),
 # valid only while the kernel's sources are unchanged (sha256 of the files)
-TRAFFIC = {"attn": {"bytes": 631519000 + 2508000, "sha": "e2d7b6d90c59433b", "files": ("tr_attn.cu", "tr_sm100.cuh")}}
+TRAFFIC = {"attn": {"bytes": 631514000 + 2531000, "sha": "e0ee697942013f87", "files": ("tr_attn.cu", "tr_sm100.cuh")}}
 
 
 PRIME_CYCLES = 2_000_000   # about 1 ms of device time at the GB300's clocks

@@ -468,7 +468,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       const int T = sg.n;
       const int h = sg.g * a.G + sg.hg;
       float m_run = -INFINITY, l_run = 0.f;  // running maximum (log2 units) and sum
-      int done_here = 0;  // tiles of this segment this unit has folded into its accumulator
+      int done_here = 0;  // tiles of this segment this warpgroup has folded into its accumulator
       for (int u = 0; u < T && ok; ++u) {
         const int gtt = gt + u, sb = gtt % NSB;
         if ((gtt & 1) != grp) continue;  // the other warpgroup's tile
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
           const float m_new = fmaxf(m_run, mx);
           const bool need = m_new > m_run + kRescaleLog2;  // also true for the row's first finite maximum
           if (__any_sync(0xffffffffu, need && done_here > 0)) {
-            // O already holds this unit's earlier tiles: wait for the last PV into it, then scale it
+            // O already holds this warpgroup's earlier tiles: wait for the last PV into it, then scale it
             const int gp = gtt - GROUPS;
             if (!wwait(&bars->pv_done[gp % NSB], (gp / NSB) & 1)) {
               ok = false;
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         l_run = 0.f;
       }
       // the CTA groups that own parts of a split pair: group q owns
-      // [total*q/groups, total*(q+1)/groups); its CTA for these query heads is q*GS + cg
+      // [total*q/groups, total*(q+1)/groups); its CTA for this query head is q*GS + cg
       const long long p_total = bars->pref[a.B];
       const long long p_last = p_first + tiles_per_pair(sg.Lb, N) - 1;
       const int pc0 = range_owner(p_first, p_total, groups), pc1 = range_owner(p_last, p_total, groups);
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
       if (!wwait(&bars->ml_ready, sc & 1)) break;
       const float2 other = bars->ml_x[sc & 1][grp ^ 1][r];
       const float M = fmaxf(m_run, other.x);
-      const float wa = m_run == -INFINITY ? 0.f : ex2(m_run - M);   // this unit's accumulator
+      const float wa = m_run == -INFINITY ? 0.f : ex2(m_run - M);   // this warpgroup's accumulator
       const float wb = other.x == -INFINITY ? 0.f : ex2(other.x - M);  // the other warpgroup's
       const float l = l_run * wa + other.y * wb;
       constexpr int COLS = kD / 2;  // columns this warpgroup finishes
